@@ -1,0 +1,194 @@
+/*
+ * dflash_verify_attn.h -- C ABI of the GB300 (sm_103a) DFlash2 speculative-verification attention.
+ *
+ * What the operation is. A block of q_len drafted query tokens (FP16 Q) attends causally over a
+ * paged KV cache stored as E4M3 codes with one FP32 scale per layer for K and one for V. The
+ * context is cut into logical splits; each split keeps an FP32 running max, sum and numerator per
+ * query row, and a combine pass merges them into an FP16 output and an FP32 log-sum-exp.
+ * Sources, by page and section:
+ *   - "[Perf] Reduce DFlash2 attention cost and screen exact QK reuse", Test Plan: shape
+ *     q8 / Hq6 / Hkv1 / D256 per tensor-parallel rank, FP16 activations, E4M3 KV, FP32 state,
+ *     sixteen distinct layer KV allocations timed under CUDA-graph replay; Test Result: each layer
+ *     runs one grouped q8 attention kernel followed by one combine kernel.
+ *   - "[Perf] Reduce DFlash2 long-context verification decay", Implementation: six-head KV reuse,
+ *     vector loads, page specialisation, logical context splits with FP32 state; Purpose:
+ *     capacity 262144 tokens.
+ *   - "[Perf] Add opt-in DFlash2 schedules and numerical audits", Test Plan: E4M3 target KV,
+ *     FP32 logits/state.
+ *
+ * The math (the pages leave it implicit; this is the plain reading):
+ *   k^ = e4m3(code) * k_scale, v^ = e4m3(code) * v_scale  (OCP E4M3FN: bias 7, max 448)
+ *   query token i (0 <= i < q_len) of sequence b sits at position N - q_len + i, N = context_lens[b]
+ *   s_j = (q . k^_j) / sqrt(head_dim), visible iff 0 <= j <= N - q_len + i
+ *   lse = ln sum_visible e^{s_j}  (natural log),  out = sum_visible e^{s_j - lse} v^_j
+ *   A row with no visible key gets out = 0 and lse = -inf.
+ * Query head hq uses KV head hq / (num_q_heads / num_kv_heads).
+ *
+ * Layouts (row-major, no padding, device memory unless stated):
+ *   q            FP16  [batch, q_len, num_q_heads, head_dim]
+ *   k_pool       uint8 [num_pages, page_size, num_kv_heads, head_dim]  E4M3FN codes
+ *   v_pool       uint8 same layout as k_pool
+ *   block_table  int32 [batch, max_pages_per_seq]; logical page p of sequence b lives in
+ *                physical page block_table[b][p]; only the first ceil(N / page_size) entries of a
+ *                row are read
+ *   context_lens int32 [batch]; N, counting the q_len drafted tokens
+ *   k_scale, v_scale  one FP32 each (device scalars, so one captured graph serves every layer's
+ *                scale and a growing context)
+ *   out          FP16  [batch, q_len, num_q_heads, head_dim]
+ *   lse          FP32  [batch, q_len, num_q_heads]
+ *   workspace    caller-allocated, plan.workspace_bytes, 256-byte aligned; private layout
+ *                described by the plan (offsets below) so tests can read the split state.
+ *
+ * Conventions.
+ *   - Every call returns a dflash_status. Nothing allocates, throws, or synchronises, except
+ *     dflash_verify_attn_read_flags, which is documented as synchronous.
+ *   - run and combine are stream-ordered and capturable in a CUDA graph; they read
+ *     context_lens, k_scale and v_scale on the device.
+ *   - Host-checkable preconditions are checked in plan (shape support) and in run / combine
+ *     (null pointers, alignment, workspace size) and return DFLASH_ERR_INVALID_ARGUMENT or
+ *     DFLASH_ERR_WORKSPACE_TOO_SMALL without launching anything.
+ *   - Device-only conditions never fault. A context above plan.problem.max_context is clamped to
+ *     it, a block-table entry outside [0, num_pages) is clamped into range, and each sets a bit in
+ *     the sticky status word at the head of the workspace (DFLASH_FLAG_*). The caller zeroes that
+ *     word once when allocating the workspace (dflash_verify_attn_read_flags can clear it).
+ *   - Launch failures map to DFLASH_ERR_CUDA (cudaGetLastError, which does not synchronise).
+ */
+#ifndef DFLASH_VERIFY_ATTN_H
+#define DFLASH_VERIFY_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DFLASH_VERIFY_ATTN_VERSION 1
+
+typedef enum {
+    DFLASH_OK = 0,
+    DFLASH_ERR_INVALID_ARGUMENT = -1,
+    DFLASH_ERR_UNSUPPORTED = -2,
+    DFLASH_ERR_WORKSPACE_TOO_SMALL = -3,
+    DFLASH_ERR_CUDA = -4
+} dflash_status;
+
+/* Bits of the device status word (workspace offset 0, int32, sticky). */
+#define DFLASH_FLAG_CONTEXT_CLAMPED 0x1  /* some context_lens[b] > max_context: clamped     */
+#define DFLASH_FLAG_CONTEXT_SHORT 0x2    /* some context_lens[b] < q_len: early rows see no key */
+#define DFLASH_FLAG_PAGE_CLAMPED 0x4     /* a block-table entry outside [0, num_pages): clamped */
+
+/* Partial-attention kernel variants a plan can select. */
+#define DFLASH_KERNEL_AUTO 0
+#define DFLASH_KERNEL_SIMT 1     /* CUDA-core FP32 kernel: any supported shape */
+#define DFLASH_KERNEL_TCGEN05 2  /* tensor-core (tcgen05, TMEM) kernel */
+
+/* Shape of one layer's problem. Host struct, filled by the caller. */
+typedef struct {
+    int32_t version;           /* DFLASH_VERIFY_ATTN_VERSION */
+    int32_t batch;             /* sequences, >= 1 */
+    int32_t q_len;             /* drafted tokens per sequence, 1..8 */
+    int32_t num_q_heads;       /* Hq */
+    int32_t num_kv_heads;      /* Hkv; Hq % Hkv == 0 and q_len * Hq / Hkv <= 64 */
+    int32_t head_dim;          /* 256 */
+    int32_t page_size;         /* tokens per page; a multiple of 16 */
+    int32_t max_pages_per_seq; /* block-table row stride; >= ceil(max_context / page_size) */
+    int32_t num_pages;         /* pages in each pool (bounds for block-table entries) */
+    int32_t max_context;       /* largest N any call of this plan sees, >= 1 */
+    int32_t device;            /* CUDA ordinal whose SM count sizes the plan */
+    int32_t num_splits;        /* 0: planner's choice; > 0 forces the split count */
+    int32_t kernel;            /* DFLASH_KERNEL_*; AUTO picks the fastest supported */
+    int32_t reserved;
+} dflash_verify_attn_problem;
+
+/* Written by dflash_verify_attn_plan, read-only afterwards. Host POD; copy freely. */
+typedef struct {
+    int32_t version;
+    int32_t kernel;           /* DFLASH_KERNEL_SIMT or DFLASH_KERNEL_TCGEN05 */
+    int32_t num_splits;       /* S: splits per (sequence, KV head) */
+    int32_t tile_keys;        /* keys per pipeline tile; split boundaries are multiples of it */
+    int32_t min_split_keys;   /* lower bound on keys per split (a multiple of tile_keys) */
+    int32_t rows;             /* R = q_len * Hq / Hkv query rows per KV head */
+    int32_t threads;          /* partial-kernel block size */
+    int32_t smem_bytes;       /* partial-kernel dynamic shared memory */
+    int32_t sm_count;         /* SMs of plan.problem.device */
+    int32_t reserved;
+    size_t workspace_bytes;   /* caller allocates at least this many bytes */
+    size_t ws_state_offset;   /* float2 (m, l) [batch, Hkv, S, R]; m in log2 units */
+    size_t ws_acc_offset;     /* float numerator [batch, Hkv, S, R, head_dim], v_scale applied */
+    dflash_verify_attn_problem problem;
+} dflash_verify_attn_plan_t;
+
+/*
+ * Check the problem and choose the split count, tile and kernel for it. Host only; queries the
+ * device's SM count (cudaDeviceGetAttribute) unless problem->device < 0, in which case a
+ * 152-SM part is assumed (lets plans be built and checked without a GPU).
+ * Returns DFLASH_ERR_INVALID_ARGUMENT for a malformed problem, DFLASH_ERR_UNSUPPORTED for a
+ * well-formed shape this build has no kernel for.
+ */
+int dflash_verify_attn_plan(const dflash_verify_attn_problem* problem,
+                            dflash_verify_attn_plan_t* plan);
+
+/*
+ * Split boundaries the kernels use for a sequence of context length n (host restatement of the
+ * device rule): keys_per_split = roundup(max(ceil(n / S), min_split_keys), tile_keys), split s
+ * covers [s * keys_per_split, min(n, (s + 1) * keys_per_split)), and the first
+ * *active = ceil(n / keys_per_split) splits are non-empty (0 when n == 0). n is clamped to
+ * [0, max_context] first. starts[] receives S + 1 entries (host memory); empty splits start and
+ * end at n.
+ */
+int dflash_verify_attn_split_bounds(const dflash_verify_attn_plan_t* plan, int32_t n,
+                                    int32_t* starts, int32_t* active);
+
+/*
+ * Partial attention: for every (sequence, KV head, active split) write the split's FP32 state
+ * (m, l, numerator) into the workspace. Inputs as in the layout table above. workspace_bytes must
+ * be >= plan->workspace_bytes and the workspace 256-byte aligned; q, k_pool and v_pool must be
+ * 16-byte aligned. cuda_stream is a cudaStream_t (NULL: legacy default stream).
+ */
+int dflash_verify_attn_run(const dflash_verify_attn_plan_t* plan, const void* q,
+                           const void* k_pool, const void* v_pool, const int32_t* block_table,
+                           const int32_t* context_lens, const float* k_scale,
+                           const float* v_scale, void* workspace, size_t workspace_bytes,
+                           void* cuda_stream);
+
+/*
+ * Combine: merge the active splits' state of every query row into out (FP16, round to nearest
+ * even) and lse (FP32, natural log). Must follow dflash_verify_attn_run on the same stream with
+ * the same plan, workspace and context_lens.
+ */
+int dflash_verify_attn_combine(const dflash_verify_attn_plan_t* plan, const void* workspace,
+                               size_t workspace_bytes, const int32_t* context_lens, void* out,
+                               float* lse, void* cuda_stream);
+
+/* run followed by combine on one stream. */
+int dflash_verify_attn_forward(const dflash_verify_attn_plan_t* plan, const void* q,
+                               const void* k_pool, const void* v_pool,
+                               const int32_t* block_table, const int32_t* context_lens,
+                               const float* k_scale, const float* v_scale, void* workspace,
+                               size_t workspace_bytes, void* out, float* lse, void* cuda_stream);
+
+/*
+ * Debug export of the kernels' E4M3 decode (the same device function the tensor-core kernel uses
+ * for K and V): decoded[t] = exact value of codes[t] (NaN for S.1111.111), scaled[t] =
+ * decoded[t] * *scale rounded once to FP32. n >= 0 elements; all pointers device memory;
+ * scaled may be NULL.
+ */
+int dflash_verify_attn_debug_dequant(const uint8_t* codes, int64_t n, const float* scale,
+                                     float* decoded, float* scaled, void* cuda_stream);
+
+/*
+ * Copy the workspace status word (DFLASH_FLAG_* bits) to *flags_host, optionally zeroing it.
+ * Synchronises cuda_stream; not for use inside graph capture.
+ */
+int dflash_verify_attn_read_flags(const void* workspace, int32_t* flags_host, int clear,
+                                  void* cuda_stream);
+
+/* Static text for a dflash_status value. */
+const char* dflash_verify_attn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH_VERIFY_ATTN_H */

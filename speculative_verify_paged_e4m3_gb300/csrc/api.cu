@@ -1,0 +1,291 @@
+// api.cu -- the C ABI: planner, argument checks, launches, debug export, status text.
+//
+// The split planner replaces the pages' fixed "80 logical splits" ("[Perf] Reduce DFlash2
+// long-context verification decay", Implementation; 80 matched the V100's SM count) with a split
+// count sized to this GPU's SMs, and a per-call rule that adapts the split length to the context
+// length read on the device.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "e4m3.cuh"
+
+namespace dflash {
+cudaError_t launch_simt_partial(const PartialParams& p, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+size_t simt_smem_bytes();
+}  // namespace dflash
+
+using namespace dflash;
+
+namespace {
+
+constexpr int kDefaultSmCount = 152;  // GB300
+constexpr size_t kHeaderBytes = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int host_keys_per_split(int n, const dflash_verify_attn_plan_t* plan) {
+    int64_t per = ceil_div(n, plan->num_splits);
+    if (per < plan->min_split_keys) per = plan->min_split_keys;
+    return (int)(ceil_div(per, plan->tile_keys) * plan->tile_keys);
+}
+
+int check_plan(const dflash_verify_attn_plan_t* plan) {
+    if (!plan || plan->version != DFLASH_VERIFY_ATTN_VERSION) return DFLASH_ERR_INVALID_ARGUMENT;
+    if (plan->num_splits < 1 || plan->tile_keys < 1 || plan->rows < 1)
+        return DFLASH_ERR_INVALID_ARGUMENT;
+    return DFLASH_OK;
+}
+
+PartialParams partial_params(const dflash_verify_attn_plan_t* plan, const void* q,
+                             const void* k_pool, const void* v_pool, const int32_t* block_table,
+                             const int32_t* context_lens, const float* k_scale,
+                             const float* v_scale, void* workspace) {
+    const dflash_verify_attn_problem& pr = plan->problem;
+    PartialParams p;
+    p.q = static_cast<const __half*>(q);
+    p.k_pool = static_cast<const uint8_t*>(k_pool);
+    p.v_pool = static_cast<const uint8_t*>(v_pool);
+    p.block_table = block_table;
+    p.context_lens = context_lens;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    char* ws = static_cast<char*>(workspace);
+    p.status = reinterpret_cast<int32_t*>(ws);
+    p.ws_state = reinterpret_cast<float2*>(ws + plan->ws_state_offset);
+    p.ws_acc = reinterpret_cast<float*>(ws + plan->ws_acc_offset);
+    p.batch = pr.batch;
+    p.q_len = pr.q_len;
+    p.num_q_heads = pr.num_q_heads;
+    p.num_kv_heads = pr.num_kv_heads;
+    p.group = pr.num_q_heads / pr.num_kv_heads;
+    p.rows = plan->rows;
+    p.page_size = pr.page_size;
+    p.max_pages_per_seq = pr.max_pages_per_seq;
+    p.num_pages = pr.num_pages;
+    p.max_context = pr.max_context;
+    p.num_splits = plan->num_splits;
+    p.tile_keys = plan->tile_keys;
+    p.min_split_keys = plan->min_split_keys;
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dflash_verify_attn_status_string(int status) {
+    switch (status) {
+        case DFLASH_OK: return "ok";
+        case DFLASH_ERR_INVALID_ARGUMENT: return "invalid argument";
+        case DFLASH_ERR_UNSUPPORTED: return "unsupported shape or kernel";
+        case DFLASH_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case DFLASH_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+int dflash_verify_attn_plan(const dflash_verify_attn_problem* pr,
+                            dflash_verify_attn_plan_t* plan) {
+    if (!pr || !plan) return DFLASH_ERR_INVALID_ARGUMENT;
+    if (pr->version != DFLASH_VERIFY_ATTN_VERSION) return DFLASH_ERR_INVALID_ARGUMENT;
+    if (pr->batch < 1 || pr->q_len < 1 || pr->num_q_heads < 1 || pr->num_kv_heads < 1 ||
+        pr->head_dim < 1 || pr->page_size < 1 || pr->max_pages_per_seq < 1 ||
+        pr->num_pages < 1 || pr->max_context < 1 || pr->num_splits < 0)
+        return DFLASH_ERR_INVALID_ARGUMENT;
+    if (pr->num_q_heads % pr->num_kv_heads != 0) return DFLASH_ERR_INVALID_ARGUMENT;
+    if ((int64_t)pr->max_pages_per_seq * pr->page_size < pr->max_context)
+        return DFLASH_ERR_INVALID_ARGUMENT;
+    if (pr->kernel < DFLASH_KERNEL_AUTO || pr->kernel > DFLASH_KERNEL_TCGEN05)
+        return DFLASH_ERR_INVALID_ARGUMENT;
+    if (pr->head_dim != kHeadDim) return DFLASH_ERR_UNSUPPORTED;
+    if (pr->page_size % 16 != 0) return DFLASH_ERR_UNSUPPORTED;
+    const int group = pr->num_q_heads / pr->num_kv_heads;
+    const int64_t rows = (int64_t)pr->q_len * group;
+    if (rows > kMaxRows) return DFLASH_ERR_UNSUPPORTED;
+    if (pr->kernel == DFLASH_KERNEL_TCGEN05) return DFLASH_ERR_UNSUPPORTED;
+
+    int sm_count = kDefaultSmCount;
+    if (pr->device >= 0) {
+        if (cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, pr->device) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return DFLASH_ERR_CUDA;
+        }
+    }
+
+    memset(plan, 0, sizeof(*plan));
+    plan->version = DFLASH_VERIFY_ATTN_VERSION;
+    plan->kernel = DFLASH_KERNEL_SIMT;
+    plan->tile_keys = 32;
+    plan->min_split_keys = 256;
+    plan->threads = 256;
+    plan->smem_bytes = (int32_t)simt_smem_bytes();
+    const int64_t units = (int64_t)pr->batch * pr->num_kv_heads;
+    int64_t S = pr->num_splits;
+    if (S == 0) {
+        S = ceil_div(sm_count, units);  // one wave of single-CTA-per-SM work
+        const int64_t cap = ceil_div(pr->max_context, plan->min_split_keys);
+        if (S > cap) S = cap;
+    }
+    if (S < 1) S = 1;
+    if (S > 65535) return DFLASH_ERR_UNSUPPORTED;
+    plan->num_splits = (int32_t)S;
+    plan->rows = (int32_t)rows;
+    plan->sm_count = sm_count;
+    const size_t state_bytes = (size_t)units * S * rows * sizeof(float2);
+    const size_t acc_bytes = (size_t)units * S * rows * kHeadDim * sizeof(float);
+    plan->ws_state_offset = kHeaderBytes;
+    plan->ws_acc_offset = kHeaderBytes + align_up(state_bytes, 256);
+    plan->workspace_bytes = plan->ws_acc_offset + acc_bytes;
+    plan->problem = *pr;
+    return DFLASH_OK;
+}
+
+int dflash_verify_attn_split_bounds(const dflash_verify_attn_plan_t* plan, int32_t n,
+                                    int32_t* starts, int32_t* active) {
+    int rc = check_plan(plan);
+    if (rc != DFLASH_OK) return rc;
+    if (!starts || !active) return DFLASH_ERR_INVALID_ARGUMENT;
+    if (n > plan->problem.max_context) n = plan->problem.max_context;
+    if (n < 0) n = 0;
+    const int per = host_keys_per_split(n, plan);
+    for (int s = 0; s <= plan->num_splits; ++s) {
+        int64_t st = (int64_t)s * per;
+        starts[s] = (int32_t)(st < n ? st : n);
+    }
+    *active = n > 0 ? (int32_t)ceil_div(n, per) : 0;
+    return DFLASH_OK;
+}
+
+int dflash_verify_attn_run(const dflash_verify_attn_plan_t* plan, const void* q,
+                           const void* k_pool, const void* v_pool, const int32_t* block_table,
+                           const int32_t* context_lens, const float* k_scale,
+                           const float* v_scale, void* workspace, size_t workspace_bytes,
+                           void* cuda_stream) {
+    int rc = check_plan(plan);
+    if (rc != DFLASH_OK) return rc;
+    if (!q || !k_pool || !v_pool || !block_table || !context_lens || !k_scale || !v_scale ||
+        !workspace)
+        return DFLASH_ERR_INVALID_ARGUMENT;
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+        !aligned(workspace, 256) || !aligned(block_table, 4) || !aligned(context_lens, 4))
+        return DFLASH_ERR_INVALID_ARGUMENT;
+    if (workspace_bytes < plan->workspace_bytes) return DFLASH_ERR_WORKSPACE_TOO_SMALL;
+    const PartialParams p = partial_params(plan, q, k_pool, v_pool, block_table, context_lens,
+                                           k_scale, v_scale, workspace);
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    cudaError_t e = cudaErrorInvalidValue;
+    if (plan->kernel == DFLASH_KERNEL_SIMT) e = launch_simt_partial(p, stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return plan->kernel == DFLASH_KERNEL_SIMT ? DFLASH_ERR_CUDA : DFLASH_ERR_UNSUPPORTED;
+    }
+    return DFLASH_OK;
+}
+
+int dflash_verify_attn_combine(const dflash_verify_attn_plan_t* plan, const void* workspace,
+                               size_t workspace_bytes, const int32_t* context_lens, void* out,
+                               float* lse, void* cuda_stream) {
+    int rc = check_plan(plan);
+    if (rc != DFLASH_OK) return rc;
+    if (!workspace || !context_lens || !out || !lse) return DFLASH_ERR_INVALID_ARGUMENT;
+    if (!aligned(workspace, 256) || !aligned(out, 8) || !aligned(lse, 4))
+        return DFLASH_ERR_INVALID_ARGUMENT;
+    if (workspace_bytes < plan->workspace_bytes) return DFLASH_ERR_WORKSPACE_TOO_SMALL;
+    const dflash_verify_attn_problem& pr = plan->problem;
+    const char* ws = static_cast<const char*>(workspace);
+    CombineParams c;
+    c.ws_state = reinterpret_cast<const float2*>(ws + plan->ws_state_offset);
+    c.ws_acc = reinterpret_cast<const float*>(ws + plan->ws_acc_offset);
+    c.context_lens = context_lens;
+    c.out = static_cast<__half*>(out);
+    c.lse = lse;
+    c.batch = pr.batch;
+    c.q_len = pr.q_len;
+    c.num_q_heads = pr.num_q_heads;
+    c.num_kv_heads = pr.num_kv_heads;
+    c.group = pr.num_q_heads / pr.num_kv_heads;
+    c.rows = plan->rows;
+    c.max_context = pr.max_context;
+    c.num_splits = plan->num_splits;
+    c.tile_keys = plan->tile_keys;
+    c.min_split_keys = plan->min_split_keys;
+    if (launch_combine(c, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return DFLASH_ERR_CUDA;
+    }
+    return DFLASH_OK;
+}
+
+int dflash_verify_attn_forward(const dflash_verify_attn_plan_t* plan, const void* q,
+                               const void* k_pool, const void* v_pool,
+                               const int32_t* block_table, const int32_t* context_lens,
+                               const float* k_scale, const float* v_scale, void* workspace,
+                               size_t workspace_bytes, void* out, float* lse, void* cuda_stream) {
+    int rc = dflash_verify_attn_run(plan, q, k_pool, v_pool, block_table, context_lens, k_scale,
+                                    v_scale, workspace, workspace_bytes, cuda_stream);
+    if (rc != DFLASH_OK) return rc;
+    return dflash_verify_attn_combine(plan, workspace, workspace_bytes, context_lens, out, lse,
+                                      cuda_stream);
+}
+
+}  // extern "C"
+
+namespace dflash {
+
+__global__ void debug_dequant_kernel(const uint8_t* codes, int64_t n, const float* scale,
+                                     float* decoded, float* scaled) {
+    const float sc = scaled ? __ldg(scale) : 0.f;
+    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < n;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const uint32_t c = codes[t];
+        float v = e4m3_to_float(c);
+        if ((c & 0x7Fu) == 0x7Fu) v = (c & 0x80u) ? -NAN : NAN;
+        decoded[t] = v;
+        if (scaled) scaled[t] = __fmul_rn(v, sc);
+    }
+}
+
+}  // namespace dflash
+
+extern "C" int dflash_verify_attn_debug_dequant(const uint8_t* codes, int64_t n,
+                                                const float* scale, float* decoded,
+                                                float* scaled, void* cuda_stream) {
+    if (n < 0 || (n > 0 && (!codes || !decoded)) || (scaled && !scale))
+        return DFLASH_ERR_INVALID_ARGUMENT;
+    if (n == 0) return DFLASH_OK;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    debug_dequant_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(cuda_stream)>>>(
+        codes, n, scale, decoded, scaled);
+    if (cudaGetLastError() != cudaSuccess) return DFLASH_ERR_CUDA;
+    return DFLASH_OK;
+}
+
+extern "C" int dflash_verify_attn_read_flags(const void* workspace, int32_t* flags_host,
+                                             int clear, void* cuda_stream) {
+    if (!workspace || !flags_host) return DFLASH_ERR_INVALID_ARGUMENT;
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        goto fail;
+    if (clear && cudaMemsetAsync(const_cast<void*>(workspace), 0, sizeof(int32_t), stream) !=
+                     cudaSuccess)
+        goto fail;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) goto fail;
+    *flags_host = v;
+    return DFLASH_OK;
+fail:
+    cudaGetLastError();
+    return DFLASH_ERR_CUDA;
+}

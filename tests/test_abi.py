@@ -1,0 +1,148 @@
+"""The C ABI without a GPU: symbols, struct layout, planner results and error statuses."""
+import ctypes
+import math
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def B():
+    from speculative_verify_paged_e4m3_gb300 import binding, build
+    build.build()
+    return binding
+
+
+def declared_functions():
+    names = set()
+    for f in os.listdir(HEADER_DIR):
+        if f.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, f)).read()
+            names |= set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(dflash_\w+)\s*\(", text,
+                                    re.M))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(B):
+    names = declared_functions()
+    assert len(names) >= 8
+    lib = B.load_library()
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert set(B.EXPORTED) <= set(names)
+
+
+def test_struct_layout_matches_c(B, tmp_path):
+    prog = tmp_path / "sizes.c"
+    prog.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "dflash_verify_attn.h"\n'
+        "int main(void){printf(\"%zu %zu %zu %zu %zu\\n\", sizeof(dflash_verify_attn_problem),"
+        " sizeof(dflash_verify_attn_plan_t), offsetof(dflash_verify_attn_plan_t, workspace_bytes),"
+        " offsetof(dflash_verify_attn_plan_t, ws_acc_offset),"
+        " offsetof(dflash_verify_attn_plan_t, problem)); return 0;}\n")
+    exe = tmp_path / "sizes"
+    subprocess.run(["gcc", "-I", HEADER_DIR, str(prog), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    assert got == [ctypes.sizeof(B.Problem), ctypes.sizeof(B.Plan),
+                   B.Plan.workspace_bytes.offset, B.Plan.ws_acc_offset.offset,
+                   B.Plan.problem.offset]
+
+
+def problem(B, **kw):
+    args = dict(batch=1, q_len=8, num_q_heads=6, num_kv_heads=1, head_dim=256, page_size=16,
+                max_pages_per_seq=16384, num_pages=16384, max_context=262144, device=-1)
+    args.update(kw)
+    return B.make_problem(**args)
+
+
+def test_plan_q8_capacity(B):
+    plan = B.dflash_verify_attn_plan(problem(B))
+    assert plan.rows == 48 and plan.num_splits >= 1
+    assert plan.sm_count == 152
+    assert plan.workspace_bytes >= plan.ws_acc_offset + plan.num_splits * 48 * 256 * 4
+    assert plan.ws_state_offset % 256 == 0 and plan.ws_acc_offset % 256 == 0
+    assert plan.ws_acc_offset >= plan.ws_state_offset + plan.num_splits * 48 * 8
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(version=2), -1),
+    (dict(batch=0), -1),
+    (dict(q_len=0), -1),
+    (dict(num_q_heads=5, num_kv_heads=2), -1),
+    (dict(max_pages_per_seq=10), -1),
+    (dict(max_context=0), -1),
+    (dict(num_splits=-1), -1),
+    (dict(kernel=7), -1),
+    (dict(head_dim=128), -2),
+    (dict(page_size=24, max_pages_per_seq=20000), -2),
+    (dict(q_len=9, num_q_heads=8), -2),  # 72 rows per KV head
+])
+def test_plan_errors(B, kw, status):
+    pr = problem(B, **{k: v for k, v in kw.items() if k != "version"})
+    if "version" in kw:
+        pr.version = kw["version"]
+    assert B.dflash_verify_attn_plan_status(pr) == status
+
+
+@pytest.mark.parametrize("n", [0, 1, 7, 8, 100, 1024, 32768, 131072, 261888, 262144, 300000])
+def test_split_bounds_rule(B, n):
+    plan = B.dflash_verify_attn_plan(problem(B))
+    starts, active = B.dflash_verify_attn_split_bounds(plan, n)
+    S = plan.num_splits
+    nn = min(max(n, 0), 262144)
+    assert len(starts) == S + 1 and starts[0] == 0 and starts[-1] == nn
+    assert all(a <= b for a, b in zip(starts, starts[1:]))
+    per = max(math.ceil(nn / S), plan.min_split_keys)
+    per = math.ceil(per / plan.tile_keys) * plan.tile_keys
+    assert active == (math.ceil(nn / per) if nn else 0)
+    for s in range(S):
+        assert starts[s] == min(nn, s * per)
+        if s < active:
+            assert starts[s + 1] > starts[s] and starts[s] % plan.tile_keys == 0
+        else:
+            assert starts[s + 1] == starts[s] == nn
+
+
+def test_forced_split_count(B):
+    plan = B.dflash_verify_attn_plan(problem(B, num_splits=300))
+    assert plan.num_splits == 300
+    starts, active = B.dflash_verify_attn_split_bounds(plan, 261888)
+    assert active <= 300 and starts[active] == 261888
+
+
+def test_run_rejects_bad_arguments_without_launching(B):
+    plan = B.dflash_verify_attn_plan(problem(B))
+    lib = B.load_library()
+    # null pointers
+    rc = lib.dflash_verify_attn_run(ctypes.byref(plan), None, None, None, None, None, None, None,
+                                    None, 0, None)
+    assert rc == B.DFLASH_ERR_INVALID_ARGUMENT
+    # misaligned q (no device memory is touched: arguments are checked first)
+    fake = 4096
+    rc = lib.dflash_verify_attn_run(ctypes.byref(plan), fake + 2, fake, fake, fake, fake, fake,
+                                    fake, fake, plan.workspace_bytes, None)
+    assert rc == B.DFLASH_ERR_INVALID_ARGUMENT
+    # workspace too small
+    rc = lib.dflash_verify_attn_run(ctypes.byref(plan), fake, fake, fake, fake, fake, fake,
+                                    fake, fake, plan.workspace_bytes - 1, None)
+    assert rc == B.DFLASH_ERR_WORKSPACE_TOO_SMALL
+    rc = lib.dflash_verify_attn_combine(ctypes.byref(plan), fake, plan.workspace_bytes - 1,
+                                        fake, fake, fake, None)
+    assert rc == B.DFLASH_ERR_WORKSPACE_TOO_SMALL
+    bad = B.Plan()
+    rc = lib.dflash_verify_attn_combine(ctypes.byref(bad), fake, 1 << 30, fake, fake, fake, None)
+    assert rc == B.DFLASH_ERR_INVALID_ARGUMENT
+    rc = lib.dflash_verify_attn_debug_dequant(None, -1, None, None, None, None)
+    assert rc == B.DFLASH_ERR_INVALID_ARGUMENT
+
+
+def test_status_strings(B):
+    for s in (0, -1, -2, -3, -4):
+        assert B.status_string(s)
+    assert B.status_string(12345) == "unknown status"

@@ -1,0 +1,205 @@
+"""CUDA path against the oracle, element by element, through the C ABI (needs a GPU)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import compare, gpu_forward, oracle_forward, to_device, to_np
+from speculative_verify_paged_e4m3_gb300 import workload as W
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = [1]  # DFLASH_KERNEL_SIMT
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_verify_paged_e4m3_gb300 import build
+    build.build()
+
+
+def small(name, context, q_len=8, Hq=6, Hkv=1, P=16, pool_factor=1.5, seed=0, boost=0.0,
+          max_context=0):
+    return W.Workload(name, layers=1, context=tuple(context), q_len=q_len, num_q_heads=Hq,
+                      num_kv_heads=Hkv, page_size=P, pool_factor=pool_factor,
+                      boost_frac=boost, boost_factor=4.0, seed_base=90000 + seed,
+                      max_context=max_context)
+
+
+def check(w, kernel, num_splits=0, layer=0):
+    inp = W.make_layer(w, layer, device="cpu")
+    dev = to_device(inp)
+    att, out, lse = gpu_forward(dev, num_splits=num_splits, kernel=kernel)
+    ref_out, ref_lse = oracle_forward(inp)
+    compare(to_np(out), to_np(lse), ref_out, ref_lse, what=w.name)
+    flags = att.workspace_views()[0].item()
+    assert flags & 0x4 == 0, "a block-table entry inside the context was out of range?"
+    return att, inp, dev, out, lse
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_config0_full(kernel):
+    check(W.config0(), kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("q_len", range(1, 9))
+@pytest.mark.parametrize("n", [1, 9, 100, 1031, 4100])
+def test_tail_shapes_ragged_contexts(kernel, q_len, n):
+    if n < q_len:
+        n = q_len
+    check(small(f"q{q_len}_n{n}", [n], q_len=q_len, seed=q_len * 7 + n), kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 64, 500])
+def test_forced_split_counts(kernel, splits):
+    check(small(f"splits{splits}", [3000], seed=splits), kernel, num_splits=splits)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("P,n", [(16, 777), (32, 1000), (48, 999), (64, 2049), (3296, 7000)])
+def test_page_sizes(kernel, P, n):
+    check(small(f"P{P}", [n], P=P, seed=P), kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_batch_ragged_two_kv_heads(kernel):
+    check(small("b3_hkv2", [1500, 17, 640], Hq=12, Hkv=2, seed=3), kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_sixty_four_rows(kernel):
+    check(small("g8_q8", [900], Hq=8, Hkv=1, seed=5), kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_peaked_softmax(kernel):
+    check(small("boost", [5000], P=64, seed=11, boost=0.05), kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_workspace_state_matches_oracle_partials(kernel):
+    w = small("partials", [2500], seed=21)
+    att, inp, dev, out, lse = check(w, kernel, num_splits=5)
+    from speculative_verify_paged_e4m3_gb300 import binding as B
+    starts, active = B.dflash_verify_attn_split_bounds(att.plan, 2500)
+    sb = np.array([starts], dtype=np.int32)
+    m, l, acc = oracle.load().verify_attn_partials(
+        to_np(inp["q"]), to_np(inp["k_pool"]), to_np(inp["v_pool"]), to_np(inp["block_table"]),
+        to_np(inp["context_lens"]), inp["k_scale"].item(), inp["v_scale"].item(), sb)
+    _, state, gacc = att.workspace_views()
+    state = to_np(state).astype(np.float64)
+    gacc = to_np(gacc).astype(np.float64)
+    gm = state[..., 0] / math.log2(math.e)  # kernel keeps m in log2 units
+    gl = state[..., 1]
+    for s in range(active):
+        for r in range(att.plan.rows):
+            om, ol, oa = m[0, 0, s, r], l[0, 0, s, r], acc[0, 0, s, r]
+            if om == -np.inf:
+                assert gm[0, 0, s, r] == -np.inf and gl[0, 0, s, r] == 0
+                continue
+            # the state is defined up to its reference max: compare l * e^m, and the split's
+            # own normalised output acc / l with the output tolerance
+            scale = math.exp(gm[0, 0, s, r] - om)
+            assert abs(gl[0, 0, s, r] * scale - ol) <= 1e-4 * ol, (s, r)
+            np.testing.assert_allclose(gacc[0, 0, s, r] / gl[0, 0, s, r], oa / ol, rtol=0,
+                                       atol=2e-3, err_msg=f"split {s} row {r}")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_context_shorter_than_q_len_and_empty(kernel):
+    from speculative_verify_paged_e4m3_gb300 import binding as B
+    w = small("short", [3, 0, 40], q_len=8, seed=31)
+    inp = W.make_layer(w, 0, device="cpu")
+    att, out, lse = gpu_forward(to_device(inp), kernel=kernel)
+    ref_out, ref_lse = oracle_forward(inp)
+    compare(to_np(out), to_np(lse), ref_out, ref_lse, what="short")
+    assert np.all(np.isneginf(to_np(lse)[1]))
+    assert np.all(to_np(out)[1] == 0)
+    assert att.workspace_views()[0].item() & B.DFLASH_FLAG_CONTEXT_SHORT
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_context_above_plan_is_clamped(kernel):
+    from speculative_verify_paged_e4m3_gb300 import binding as B
+    w = small("clamp", [1200], seed=41)
+    inp = W.make_layer(w, 0, device="cpu")
+    att, out, lse = gpu_forward(to_device(inp), kernel=kernel, max_context=1000)
+    ref_out, ref_lse = oracle_forward(inp, context_override=[1000])
+    compare(to_np(out), to_np(lse), ref_out, ref_lse, what="clamp")
+    assert att.workspace_views()[0].item() & B.DFLASH_FLAG_CONTEXT_CLAMPED
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_out_of_range_page_is_clamped_and_flagged(kernel):
+    from speculative_verify_paged_e4m3_gb300 import binding as B
+    w = small("badpage", [500], seed=51, pool_factor=1.0)
+    inp = W.make_layer(w, 0, device="cpu")
+    num_pages = inp["k_pool"].shape[0]
+    inp["block_table"][0, 3] = num_pages + 100  # clamps to the last page
+    inp["block_table"][0, 5] = -4               # clamps to page 0
+    att, out, lse = gpu_forward(to_device(inp), kernel=kernel)
+    fixed = dict(inp)
+    fixed["block_table"] = inp["block_table"].clone()
+    fixed["block_table"][0, 3] = num_pages - 1
+    fixed["block_table"][0, 5] = 0
+    ref_out, ref_lse = oracle_forward(fixed)
+    compare(to_np(out), to_np(lse), ref_out, ref_lse, what="badpage")
+    assert att.workspace_views()[0].item() & B.DFLASH_FLAG_PAGE_CLAMPED
+    assert B.dflash_verify_attn_read_flags(att.workspace, clear=True) & 0x4
+    assert B.dflash_verify_attn_read_flags(att.workspace) == 0
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_deterministic_and_canaries_intact(kernel):
+    from speculative_verify_paged_e4m3_gb300 import binding as B
+    w = small("canary", [3333], seed=61)
+    dev = to_device(W.make_layer(w, 0, device="cpu"))
+    Bq, q_len, Hq, D = dev["q"].shape
+    guard = 4096
+    att = B.VerifyAttention(Bq, q_len, Hq, 1, D, 16, dev["block_table"].shape[1],
+                            dev["k_pool"].shape[0], 3333, kernel=kernel)
+    ws_bytes = att.plan.workspace_bytes
+    big_ws = torch.full((ws_bytes + 2 * guard,), 0xA5, dtype=torch.uint8, device="cuda")
+    big_ws[guard:guard + 4].zero_()
+    att.workspace = big_ws[guard:guard + ws_bytes]
+    n_out = Bq * q_len * Hq * D
+    out_buf = torch.full((n_out + 2 * guard,), 7.0, dtype=torch.float16, device="cuda")
+    lse_buf = torch.full((Bq * q_len * Hq + 2 * guard,), 7.0, dtype=torch.float32, device="cuda")
+    outs = []
+    for _ in range(2):
+        out = out_buf[guard:guard + n_out].view(Bq, q_len, Hq, D)
+        lse = lse_buf[guard:guard + Bq * q_len * Hq].view(Bq, q_len, Hq)
+        att(dev["q"], dev["k_pool"], dev["v_pool"], dev["block_table"], dev["context_lens"],
+            dev["k_scale"], dev["v_scale"], out=out, lse=lse)
+        torch.cuda.synchronize()
+        outs.append((out.clone(), lse.clone()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    for buf, val in ((out_buf, 7.0), (lse_buf, 7.0)):
+        assert torch.all(buf[:guard] == val) and torch.all(buf[-guard:] == val)
+    assert torch.all(big_ws[:guard] == 0xA5) and torch.all(big_ws[-guard:] == 0xA5)
+
+
+def test_debug_dequant_bit_exact():
+    from speculative_verify_paged_e4m3_gb300 import binding as B
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8).repeat(3).cuda()
+    for sc in (1.0, 0.0123, 3.7e-3, 448.0 / 7.0):
+        scale = torch.tensor([sc], dtype=torch.float32, device="cuda")
+        dec = torch.empty(codes.shape, dtype=torch.float32, device="cuda")
+        scd = torch.empty_like(dec)
+        B.dflash_verify_attn_debug_dequant(codes, scale, dec, scd)
+        torch.cuda.synchronize()
+        ref = oracle.load().e4m3_decode(to_np(codes))
+        g = to_np(dec).astype(np.float64)
+        nan = np.isnan(ref)
+        assert np.array_equal(np.isnan(g), nan)
+        assert np.array_equal(g[~nan], ref[~nan])
+        assert np.array_equal(np.signbit(g[~nan]), np.signbit(ref[~nan]))
+        sc32 = np.float64(np.float32(sc))
+        ref_scaled = (ref[~nan] * sc32).astype(np.float32)  # exact product, one rounding
+        assert np.array_equal(to_np(scd)[~nan].view(np.uint32), ref_scaled.view(np.uint32))
