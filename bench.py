@@ -1,0 +1,390 @@
+"""Benchmark: 16-layer q8 verification attention over a paged E4M3 KV cache on one GB300.
+
+A step is one pass of the whole path (16 layers x [partial attention + combine]) over the
+workload's resident inputs, replayed from one CUDA graph. Default workload: 16 layers, batch 1,
+q_len 8, Hq 6, Hkv 1, D 256, context 261888 (the capacity boundary window), page 16, shuffled
+block tables, 2.15 GB of distinct E4M3 K/V per step (far larger than L2, so no flush is needed;
+smaller workloads get a 512 MB L2 flush between timed steps).
+
+Prints one JSON line (rank 0). `--impl reference` times the FP64 CPU oracle instead, on a bounded
+sample of the same workload, scaled to the same unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "16-layer q8 verify-attention ms at 32K-262K ctx; achieved HBM GB/s vs peak"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="c3", help="c0|c1|c2|c3|c4:<q_len>:<context>")
+    ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05")
+    ap.add_argument("--splits", type=int, default=0, help="force the split count (0: planner)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def workload(name):
+    from speculative_verify_paged_e4m3_gb300 import workload as W
+    if name.startswith("c4"):
+        _, q, n = name.split(":")
+        return W.config4(int(q), int(n))
+    return {"c0": W.config0, "c1": W.config1, "c2": W.config2, "c3": W.config3}[name]()
+
+
+def measured_peak():
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_verify_paged_e4m3_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_tag, workload_name, src_hash):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current sources."""
+    path = os.path.join(PROFILES, f"{kernel_tag}_{workload_name}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    hm = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    if not m or not hm or hm.group(1) != src_hash:
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        try:
+            lines = open(self.path).read().strip().splitlines()
+        except OSError:
+            lines = []
+        for line in lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_ms_per_step(w, layers_sample, rows_note, steps=1):
+    """Time the FP64 oracle on whole sample layers; scale to ms per len(w.layers) layers."""
+    import numpy as np
+
+    import oracle
+    from speculative_verify_paged_e4m3_gb300 import workload as W
+    orc = oracle.load()
+    data = [W.make_layer(w, l, device="cpu") for l in layers_sample]
+    args = [(d["q"].numpy(), d["k_pool"].numpy(), d["v_pool"].numpy(), d["block_table"].numpy(),
+             d["context_lens"].numpy(), float(d["k_scale"].item()), float(d["v_scale"].item()))
+            for d in data]
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        for a in args:
+            orc.verify_attn(*a)
+        times.append(time.perf_counter() - t0)
+    per_layer = statistics.median(times) / len(layers_sample)
+    return per_layer * w.layers * 1e3, orc.num_threads(), times
+
+
+def run_reference(args, rank, world):
+    w = workload(args.config)
+    if rank != 0:
+        return
+    total_steps = args.warmup + args.steps
+    import oracle
+    from speculative_verify_paged_e4m3_gb300 import workload as W
+    orc = oracle.load()
+    d = W.make_layer(w, 0, device="cpu")
+    a = (d["q"].numpy(), d["k_pool"].numpy(), d["v_pool"].numpy(), d["block_table"].numpy(),
+         d["context_lens"].numpy(), float(d["k_scale"].item()), float(d["v_scale"].item()))
+    times = []
+    for s in range(total_steps):
+        t0 = time.perf_counter()
+        orc.verify_attn(*a)
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            times.append(dt * w.layers * 1e3)
+    ms = statistics.mean(times)
+    sample = (f"each step: layer 0 of {w.name} (all {w.q_len * w.num_q_heads} query rows, "
+              f"{w.context[0]} keys) through the oracle, scaled x{w.layers} to 16 layers")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(ms, 3), "unit": "ms",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "layers": w.layers},
+        "cpu_baseline": {"value": round(ms, 3), "unit": "ms", "cores": orc.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(ms, 3), "unit": "ms", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from speculative_verify_paged_e4m3_gb300 import binding as B
+    from speculative_verify_paged_e4m3_gb300 import build as build_mod
+    from speculative_verify_paged_e4m3_gb300.runner import LayerStack, algorithmic_bytes
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    build_mod.build()
+    w = workload(args.config)
+    stack = LayerStack(w, device=dev, num_splits=args.splits, kernel=args.kernel)
+    plan = stack.plan
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = None
+    if w.kv_bytes_per_layer() * w.layers < 4 * l2_bytes:
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stack.capture()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        stack.replay()
+    barrier()
+
+    # timed region: K graph replays, CUDA events on the replay stream
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    with clocks:
+        barrier()
+        for s in range(args.steps):
+            if flush is not None:
+                flush.fill_(s & 0xFF)
+            starts[s].record()
+            stack.replay()
+            ends[s].record()
+        barrier()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # attribution pass: the same launches, eager, with events around every kernel
+    nl = len(stack.layers)
+    pe = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(nl)] for _ in range(args.steps)]
+    ce = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(nl)] for _ in range(args.steps)]
+    for _ in range(max(1, args.warmup)):
+        stack.launch()
+    barrier()
+    for s in range(args.steps):
+        if flush is not None:
+            flush.fill_(s & 0xFF)
+        stack.launch_timed(pe[s], ce[s])
+    barrier()
+    partial_ms = statistics.mean(a.elapsed_time(b) for row in pe for a, b in row)
+    combine_ms = statistics.mean(a.elapsed_time(b) for row in ce for a, b in row)
+
+    # end to end through the public API: per step, H2D of the step's inputs from pinned host
+    # memory (Q, block tables, context lengths, scales of all layers), the 16 layers, and D2H of
+    # the outputs and LSEs; the KV cache stays resident (it is the model's state, not an input)
+    e2e = None
+    if not args.no_e2e:
+        host_in = [{k: lay[k].cpu().pin_memory() for k in
+                    ("q", "block_table", "context_lens", "k_scale", "v_scale")}
+                   for lay in stack.layers]
+        host_out = [(o.cpu().pin_memory(), l.cpu().pin_memory())
+                    for o, l in zip(stack.outs, stack.lses)]
+        h2d = sum(t.numel() * t.element_size() for d in host_in for t in d.values())
+        d2h = sum(o.numel() * o.element_size() + l.numel() * l.element_size()
+                  for o, l in host_out)
+
+        def e2e_step():
+            for lay, hin in zip(stack.layers, host_in):
+                for k, t in hin.items():
+                    lay[k].copy_(t, non_blocking=True)
+            stack.launch()
+            for (o, l), (ho, hl) in zip(zip(stack.outs, stack.lses), host_out):
+                ho.copy_(o, non_blocking=True)
+                hl.copy_(l, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        barrier()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for s in range(args.steps):
+            if flush is not None:
+                flush.fill_(s & 0xFF)
+            ev[s][0].record()
+            e2e_step()
+            ev[s][1].record()
+        barrier()
+        e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    nbytes = algorithmic_bytes(w, plan)
+    peak, peak_kind = measured_peak()
+    achieved = nbytes["partial"] / (partial_ms * 1e-3) / 1e9
+    src_hash = kernel_source_hash()
+    ktag = {1: "simt_partial", 2: "tc_partial"}.get(plan.kernel, "partial")
+    traffic = ncu_traffic(ktag, w.name, src_hash)
+    step_bytes = (nbytes["partial"] + nbytes["combine"]) * nl
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample_layers = [0, 1]
+        cms, cores, _ = oracle_ms_per_step(w, sample_layers, "all rows")
+        cpu = {"value": round(cms, 1), "unit": "ms", "cores": cores, "kind": "oracle",
+               "sample": f"layers {sample_layers} of {w.name}, all "
+                         f"{w.q_len * w.num_q_heads} query rows, FP64 oracle; time per layer "
+                         f"x {w.layers}"}
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": round(ms, 4),
+        "unit": "ms",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32" if plan.kernel == B.DFLASH_KERNEL_SIMT else "f16*f16->f32",
+        "data": "synthetic",
+        "config": {
+            "workload": w.name, "layers": w.layers, "batch": w.batch, "q_len": w.q_len,
+            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "context": list(w.context), "page_size": w.page_size,
+            "kv_gb_per_step": round(w.kv_bytes_per_layer() * w.layers / 1e9, 4),
+            "l2": ("512 MB flush between timed steps" if flush is not None else
+                   "inputs larger than L2 (distinct KV per layer)"),
+            "kernel": ktag, "num_splits": plan.num_splits,
+            "active_splits": nbytes["active_splits"], "timing": "CUDA graph replay of 16 layers",
+        },
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "peak_kind": peak_kind, "kernel": ktag,
+            "kernel_ms": round(partial_ms, 5), "bytes_per_launch": nbytes["partial"],
+        },
+        "step_hbm_gbs": round(step_bytes / (ms * 1e-3) / 1e9, 1),
+        "step_frac_of_peak": round(step_bytes / (ms * 1e-3) / 1e9 / peak, 4),
+        "combine_kernel_ms": round(combine_ms, 5),
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * nl * args.steps,
+        "clocks": clocks.summary(),
+        "kernel_source_hash": src_hash,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
