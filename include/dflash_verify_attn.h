@@ -184,6 +184,26 @@ int dflash_verify_attn_debug_dequant(const uint8_t* codes, int64_t n, const floa
 int dflash_verify_attn_read_flags(const void* workspace, int32_t* flags_host, int clear,
                                   void* cuda_stream);
 
+/*
+ * run followed by combine with the split workspace taken from a 16 MiB device array built into
+ * the library instead of caller memory. The pages have no counterpart: this entry point exists
+ * for callers that may not allocate device memory (a plugin whose device memory belongs to a host
+ * framework's allocator, a runtime that freezes its memory pool after start-up, a loop that must
+ * never enter the allocator). They still pass every input and output; nothing here allocates.
+ * Limits and behaviour: plan->workspace_bytes must be <= 16 MiB, else
+ * DFLASH_ERR_WORKSPACE_TOO_SMALL and nothing is launched. The first call on a device (with that
+ * device current) looks up the array's device address once; make it before any stream capture.
+ * All calls share the array: the status word at its head is zeroed at the start of each call and
+ * is not reported, and calls whose kernels overlap on the GPU race on the array. The array stays
+ * allocated on every device that loaded the library until the process exits.
+ */
+int dflash_verify_attn_forward_static_scratch(const dflash_verify_attn_plan_t* plan,
+                                              const void* q, const void* k_pool,
+                                              const void* v_pool, const int32_t* block_table,
+                                              const int32_t* context_lens, const float* k_scale,
+                                              const float* v_scale, void* out, float* lse,
+                                              void* cuda_stream);
+
 /* Static text for a dflash_status value. */
 const char* dflash_verify_attn_status_string(int status);
 

@@ -36,6 +36,7 @@ EXPORTED = (
     "dflash_verify_attn_forward",
     "dflash_verify_attn_debug_dequant",
     "dflash_verify_attn_read_flags",
+    "dflash_verify_attn_forward_static_scratch",
     "dflash_verify_attn_status_string",
 )
 
@@ -90,6 +91,7 @@ def load_library() -> ctypes.CDLL:
             lib.dflash_verify_attn_run.argtypes = [pp] + [vp] * 8 + [sz, vp]
             lib.dflash_verify_attn_combine.argtypes = [pp, vp, sz, vp, vp, vp, vp]
             lib.dflash_verify_attn_forward.argtypes = [pp] + [vp] * 8 + [sz, vp, vp, vp]
+            lib.dflash_verify_attn_forward_static_scratch.argtypes = [pp] + [vp] * 10
             lib.dflash_verify_attn_debug_dequant.argtypes = [vp, i64, vp, vp, vp, vp]
             lib.dflash_verify_attn_read_flags.argtypes = [vp, ctypes.POINTER(ctypes.c_int32),
                                                           ctypes.c_int, vp]
@@ -190,6 +192,19 @@ def dflash_verify_attn_forward(plan: Plan, q, k_pool, v_pool, block_table, conte
         workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse), _stream(stream))
     if check:
         _check("dflash_verify_attn_forward", rc)
+    return rc
+
+
+def dflash_verify_attn_forward_static_scratch(plan: Plan, q, k_pool, v_pool, block_table,
+                                              context_lens, k_scale, v_scale, out, lse,
+                                              stream=None, check=True) -> int:
+    """Forward pass using the library's built-in device scratch array (no workspace argument)."""
+    rc = load_library().dflash_verify_attn_forward_static_scratch(
+        ctypes.byref(plan), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+        _ptr(context_lens), _ptr(k_scale), _ptr(v_scale), _ptr(out), _ptr(lse),
+        _stream(stream))
+    if check:
+        _check("dflash_verify_attn_forward_static_scratch", rc)
     return rc
 
 
