@@ -77,6 +77,7 @@ typedef enum {
 #define DFLASH_FLAG_CONTEXT_CLAMPED 0x1  /* some context_lens[b] > max_context: clamped     */
 #define DFLASH_FLAG_CONTEXT_SHORT 0x2    /* some context_lens[b] < q_len: early rows see no key */
 #define DFLASH_FLAG_PAGE_CLAMPED 0x4     /* a block-table entry outside [0, num_pages): clamped */
+#define DFLASH_FLAG_KERNEL_TIMEOUT 0x8   /* a tensor-core kernel wait gave up; outputs invalid */
 
 /* Partial-attention kernel variants a plan can select. */
 #define DFLASH_KERNEL_AUTO 0

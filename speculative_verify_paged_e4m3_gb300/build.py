@@ -18,7 +18,7 @@ LIB_NAME = "libdflash_verify_attn.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["api.cu", "simt_partial.cu", "combine.cu", "static_scratch.cu"]
+SOURCES = ["api.cu", "simt_partial.cu", "tc_partial.cu", "combine.cu", "static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
           "-I", INCLUDE, "-I", CSRC]
@@ -60,7 +60,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             if log:
                 print(log)
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results] + ["-lcuda"]
+    cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")

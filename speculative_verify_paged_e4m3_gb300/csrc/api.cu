@@ -16,8 +16,11 @@
 
 namespace dflash {
 cudaError_t launch_simt_partial(const PartialParams& p, cudaStream_t stream);
+cudaError_t launch_tc_partial(const PartialParams& p, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 size_t simt_smem_bytes();
+size_t tc_smem_bytes();
+bool tc_supports(int rows);
 }  // namespace dflash
 
 using namespace dflash;
@@ -112,7 +115,9 @@ int dflash_verify_attn_plan(const dflash_verify_attn_problem* pr,
     const int group = pr->num_q_heads / pr->num_kv_heads;
     const int64_t rows = (int64_t)pr->q_len * group;
     if (rows > kMaxRows) return DFLASH_ERR_UNSUPPORTED;
-    if (pr->kernel == DFLASH_KERNEL_TCGEN05) return DFLASH_ERR_UNSUPPORTED;
+    const bool tc_ok = tc_supports((int)rows);
+    if (pr->kernel == DFLASH_KERNEL_TCGEN05 && !tc_ok) return DFLASH_ERR_UNSUPPORTED;
+    const bool use_tc = tc_ok && pr->kernel != DFLASH_KERNEL_SIMT;
 
     int sm_count = kDefaultSmCount;
     if (pr->device >= 0) {
@@ -125,11 +130,19 @@ int dflash_verify_attn_plan(const dflash_verify_attn_problem* pr,
 
     memset(plan, 0, sizeof(*plan));
     plan->version = DFLASH_VERIFY_ATTN_VERSION;
-    plan->kernel = DFLASH_KERNEL_SIMT;
-    plan->tile_keys = 32;
-    plan->min_split_keys = 256;
-    plan->threads = 256;
-    plan->smem_bytes = (int32_t)simt_smem_bytes();
+    if (use_tc) {
+        plan->kernel = DFLASH_KERNEL_TCGEN05;
+        plan->tile_keys = 128;
+        plan->min_split_keys = 256;
+        plan->threads = 384;
+        plan->smem_bytes = (int32_t)tc_smem_bytes();
+    } else {
+        plan->kernel = DFLASH_KERNEL_SIMT;
+        plan->tile_keys = 32;
+        plan->min_split_keys = 256;
+        plan->threads = 256;
+        plan->smem_bytes = (int32_t)simt_smem_bytes();
+    }
     const int64_t units = (int64_t)pr->batch * pr->num_kv_heads;
     int64_t S = pr->num_splits;
     if (S == 0) {
@@ -184,11 +197,16 @@ int dflash_verify_attn_run(const dflash_verify_attn_plan_t* plan, const void* q,
     const PartialParams p = partial_params(plan, q, k_pool, v_pool, block_table, context_lens,
                                            k_scale, v_scale, workspace);
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-    cudaError_t e = cudaErrorInvalidValue;
-    if (plan->kernel == DFLASH_KERNEL_SIMT) e = launch_simt_partial(p, stream);
+    cudaError_t e;
+    if (plan->kernel == DFLASH_KERNEL_SIMT)
+        e = launch_simt_partial(p, stream);
+    else if (plan->kernel == DFLASH_KERNEL_TCGEN05)
+        e = launch_tc_partial(p, stream);
+    else
+        return DFLASH_ERR_INVALID_ARGUMENT;
     if (e != cudaSuccess) {
         cudaGetLastError();
-        return plan->kernel == DFLASH_KERNEL_SIMT ? DFLASH_ERR_CUDA : DFLASH_ERR_UNSUPPORTED;
+        return DFLASH_ERR_CUDA;
     }
     return DFLASH_OK;
 }
@@ -245,14 +263,23 @@ namespace dflash {
 
 __global__ void debug_dequant_kernel(const uint8_t* codes, int64_t n, const float* scale,
                                      float* decoded, float* scaled) {
+    // pairs of consecutive codes go through the same two-code conversion the kernels use
     const float sc = scaled ? __ldg(scale) : 0.f;
-    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < n;
+    const int64_t pairs = (n + 1) / 2;
+    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < pairs;
          t += (int64_t)gridDim.x * blockDim.x) {
-        const uint32_t c = codes[t];
-        float v = e4m3_to_float(c);
-        if ((c & 0x7Fu) == 0x7Fu) v = (c & 0x80u) ? -NAN : NAN;
-        decoded[t] = v;
-        if (scaled) scaled[t] = __fmul_rn(v, sc);
+        const int64_t i0 = 2 * t;
+        const bool two = i0 + 1 < n;
+        const uint16_t c = static_cast<uint16_t>(codes[i0] | (two ? codes[i0 + 1] << 8 : 0));
+        const uint32_t f = e4m3x2_to_f16x2(c);
+        const float v0 = __half2float(__ushort_as_half(static_cast<unsigned short>(f & 0xFFFFu)));
+        const float v1 = __half2float(__ushort_as_half(static_cast<unsigned short>(f >> 16)));
+        decoded[i0] = v0;
+        if (scaled) scaled[i0] = __fmul_rn(v0, sc);
+        if (two) {
+            decoded[i0 + 1] = v1;
+            if (scaled) scaled[i0 + 1] = __fmul_rn(v1, sc);
+        }
     }
 }
 
@@ -264,7 +291,7 @@ extern "C" int dflash_verify_attn_debug_dequant(const uint8_t* codes, int64_t n,
     if (n < 0 || (n > 0 && (!codes || !decoded)) || (scaled && !scale))
         return DFLASH_ERR_INVALID_ARGUMENT;
     if (n == 0) return DFLASH_OK;
-    int64_t blocks = (n + 255) / 256;
+    int64_t blocks = ((n + 1) / 2 + 255) / 256;
     if (blocks > 4096) blocks = 4096;
     debug_dequant_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(cuda_stream)>>>(
         codes, n, scale, decoded, scaled);

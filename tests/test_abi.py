@@ -64,6 +64,7 @@ def problem(B, **kw):
 def test_plan_q8_capacity(B):
     plan = B.dflash_verify_attn_plan(problem(B))
     assert plan.rows == 48 and plan.num_splits >= 1
+    assert plan.kernel == B.DFLASH_KERNEL_TCGEN05 and plan.tile_keys == 128
     assert plan.sm_count == 152
     assert plan.workspace_bytes >= plan.ws_acc_offset + plan.num_splits * 48 * 256 * 4
     assert plan.ws_state_offset % 256 == 0 and plan.ws_acc_offset % 256 == 0
@@ -82,6 +83,7 @@ def test_plan_q8_capacity(B):
     (dict(head_dim=128), -2),
     (dict(page_size=24, max_pages_per_seq=20000), -2),
     (dict(q_len=9, num_q_heads=8), -2),  # 72 rows per KV head
+    (dict(num_q_heads=8, kernel=2), -2),  # 64 rows: above the tensor-core kernel's 48
 ])
 def test_plan_errors(B, kw, status):
     pr = problem(B, **{k: v for k, v in kw.items() if k != "version"})

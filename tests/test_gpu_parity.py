@@ -11,7 +11,7 @@ from speculative_verify_paged_e4m3_gb300 import workload as W
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = [1]  # DFLASH_KERNEL_SIMT
+KERNELS = [1, 2]  # DFLASH_KERNEL_SIMT, DFLASH_KERNEL_TCGEN05
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -62,7 +62,8 @@ def test_forced_split_counts(kernel, splits):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
-@pytest.mark.parametrize("P,n", [(16, 777), (32, 1000), (48, 999), (64, 2049), (3296, 7000)])
+@pytest.mark.parametrize("P,n", [(16, 777), (32, 1000), (48, 999), (64, 2049), (3296, 7000),
+                                 (16, 128), (16, 129), (16, 255), (16, 256)])
 def test_page_sizes(kernel, P, n):
     check(small(f"P{P}", [n], P=P, seed=P), kernel)
 
@@ -72,9 +73,10 @@ def test_batch_ragged_two_kv_heads(kernel):
     check(small("b3_hkv2", [1500, 17, 640], Hq=12, Hkv=2, seed=3), kernel)
 
 
-@pytest.mark.parametrize("kernel", KERNELS)
-def test_sixty_four_rows(kernel):
-    check(small("g8_q8", [900], Hq=8, Hkv=1, seed=5), kernel)
+def test_sixty_four_rows_auto_kernel():
+    # 64 rows per KV head is above the tensor-core kernel's 48; the planner picks the CUDA-core one
+    att, *_ = check(small("g8_q8", [900], Hq=8, Hkv=1, seed=5), 0)
+    assert att.plan.kernel == 1
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
