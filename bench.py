@@ -42,6 +42,8 @@ def parse_args():
     ap.add_argument("--config", default="c3", help="c0|c1|c2|c3|c4:<q_len>:<context>")
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05")
     ap.add_argument("--splits", type=int, default=0, help="force the split count (0: planner)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="time only the first L layers (profiling captures; 0: all)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -210,7 +212,8 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     build_mod.build()
     w = workload(args.config)
-    stack = LayerStack(w, device=dev, num_splits=args.splits, kernel=args.kernel)
+    stack = LayerStack(w, device=dev, num_splits=args.splits, kernel=args.kernel,
+                       layers=args.layers or None)
     plan = stack.plan
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = None
@@ -345,7 +348,8 @@ def run_ours(args, rank, world, local_rank):
             "l2": ("512 MB flush between timed steps" if flush is not None else
                    "inputs larger than L2 (distinct KV per layer)"),
             "kernel": ktag, "num_splits": plan.num_splits,
-            "active_splits": nbytes["active_splits"], "timing": "CUDA graph replay of 16 layers",
+            "active_splits": nbytes["active_splits"],
+            "timing": f"CUDA graph replay of {nl} layers",
         },
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
