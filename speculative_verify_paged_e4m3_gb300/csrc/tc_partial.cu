@@ -19,10 +19,12 @@
 //    Each keeps, per row, a reference max that only moves when a score exceeds it by more than 2^8
 //    (then the warpgroup rescales its O columns in tensor memory), and FP32 row sums of the
 //    unrounded probabilities, reduced across the key lanes once per split.
-//  * Warp roles: warp 0 issues the copies (TMA: lane 0 K tiles into 2 stages, lane 16 V halves of
-//    64 keys into 3 stages); warp 1 owns tensor memory and issues the MMAs; warps 2-3 decode V
-//    into 32-key FP16 stages (2 deep); warps 4-11 stage the Q terms (while the first copies are
-//    in flight), then run the softmax (rows 0..RP/2-1 and RP/2..RP-1) and write O out.
+//  * Warp roles: warp 0 copies K tiles (TMA, 2 stages); warp 1 owns tensor memory and issues the
+//    MMAs; warp 2 copies V in 64-key halves (TMA, 3 raw stages) and warps 2-3 decode them into
+//    32-key FP16 stages (2 deep); warps 4-11 stage the Q terms (while the first
+//    copies are in flight), then run the softmax (rows 0..RP/2-1 and RP/2..RP-1) and write O out.
+//    K and V copies come from two different warps: one issuing warp tops out well below the HBM
+//    rate on this GPU (measured), two reach it.
 //    Every wait is bounded: on timeout the CTA sets DFLASH_FLAG_KERNEL_TIMEOUT, drains its copies
 //    and returns.
 #include <cuda.h>
@@ -30,6 +32,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <cstddef>
 #include <mutex>
 
 #include "common.cuh"
@@ -47,11 +50,12 @@ constexpr int kVhKeys = 32;  // keys per decoded-V stage (two MMA K steps)
 constexpr int kTerms = 3;    // E4M3 terms of Q
 constexpr int kMaxRP = 48;   // padded rows per KV head this kernel carries
 constexpr int kPN = 64;      // N of the PV MMA (rows padded to one 128-byte swizzle atom)
-constexpr int kThreads = 384;
-constexpr int kVWarps = 2;     // warps 2-3: V decode
+constexpr int kThreads = 512;
+constexpr int kVWarps = 4;     // warps 12-15: V decode
+constexpr int kVWarp0 = 12;
 constexpr int kHalf = 64;      // keys per raw-V stage
-constexpr int kVRawStages = 4;
-constexpr int kPStages = 1;
+constexpr int kVRawStages = 3;
+constexpr int kPStages = 2;
 constexpr int kVhStages = 2;
 
 constexpr uint32_t kQBytes = kTerms * kMaxRP * kHeadDim;  // 36864
@@ -79,12 +83,16 @@ struct Small {
     uint32_t tmem_base;
     int abort;
     int flag[2][2][4];            // softmax group barrier: [group][epoch parity][warp]
-    float c0[kMaxRP];             // score scale of each row (log2 units per MMA unit)
+    alignas(16) float c0[kMaxRP];    // score scale of each row (log2 units per MMA unit), read as float4
+    alignas(16) float negm[kMaxRP];  // minus the reference max of each row (+inf: no key yet), float4
     float red[2][4][kMaxRP / 2];  // per-warpgroup, per-warp partials (tile max, row sums)
     float alpha[kMaxRP];
     int rows[kRowCache];          // source row (physical page * page + slot) of chunk c of the split
 };
 constexpr uint32_t kSmemBytes = kOffSmall + sizeof(Small);
+static_assert(offsetof(Small, c0) % 16 == 0 && offsetof(Small, negm) % 16 == 0,
+              "row constants are read as float4");
+static_assert(kOffSmall % 16 == 0, "Small must start 16-byte aligned");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 // Byte offset of (row, byte k along K) in a K-major, 128-byte-swizzled operand with `rows` rows
@@ -149,14 +157,14 @@ __device__ __forceinline__ bool wg_sync(const Ctx& ctx, int wg, int wq, int& epo
     volatile int* f = ctx.sm->flag[wg][epoch & 1];
     bool done = false, v = false;
     const uint64_t t0 = globaltimer_ns();
-    while (true) {
+    for (uint32_t it = 1;; ++it) {
         const int a = f[0], b = f[1], c = f[2], d = f[3];
         if ((a >> 1) >= epoch && (b >> 1) >= epoch && (c >> 1) >= epoch && (d >> 1) >= epoch) {
             v = ((a | b | c | d) & 1) != 0;
             done = true;
             break;
         }
-        if (ctx.aborted() || globaltimer_ns() - t0 > kWaitLimitNs) break;
+        if ((it & 31) == 0 && (ctx.aborted() || globaltimer_ns() - t0 > kWaitLimitNs)) break;
     }
     __threadfence_block();
     if (!done) {
@@ -277,8 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = sm.tmem_base;
 
     if (warp == 0) {
-        // ------------------------------------------- copies (TMA): lane 0 K tiles, lane 16 V halves
-        // The two lanes run independent loops (no warp-collective operations inside).
+        // ---------------------------------------------------------------- K copies (TMA)
         if (lane == 0) {
             bool clamped = false;
             int kdone = 0;
@@ -313,40 +320,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // no copy may still be writing shared memory when the CTA retires
             for (int t = kdone - 2 < 0 ? 0 : kdone - 2; t < kdone; ++t)
                 mbar_wait(smem_u32(&sm.kfull[t & 1]), (t >> 1) & 1, &sm.abort, kWaitLimitNs);
-        } else if (lane == 16) {
-            bool clamped = false;
-            int vdone = 0;
-            for (int u = 0; u < nhalves; ++u) {
-                const int st3 = u % kVRawStages;
-                const int h0 = start + u * kHalf;
-                int rows[kHalf / kChunk];
-                int nval = 0;
-#pragma unroll
-                for (int c = 0; c < kHalf / kChunk; ++c) {
-                    const int j0 = h0 + kChunk * c;
-                    rows[c] = -1;
-                    if (j0 < end) {
-                        rows[c] = chunk_row(p, sm, b, start, j0, &clamped);
-                        ++nval;
-                    }
-                }
-                if (!ctx.wait(&sm.vfree[st3], ((u / kVRawStages) & 1) ^ 1)) break;
-                mbar_arrive_expect_tx(smem_u32(&sm.vfull[st3]), nval * kChunk * kHeadDim);
-                const uint32_t dst = smem_u32(smem + kOffVRaw + st3 * kVRawStage);
-#pragma unroll
-                for (int c = 0; c < kHalf / kChunk; ++c) {
-                    if (rows[c] < 0) continue;
-                    tma_load_2d(dst + c * 2048, &vmap, h * kHeadDim, rows[c],
-                                smem_u32(&sm.vfull[st3]));
-                    tma_load_2d(dst + c * 2048 + kVRawStage / 2, &vmap, h * kHeadDim + 128,
-                                rows[c], smem_u32(&sm.vfull[st3]));
-                }
-                vdone = u + 1;
-            }
-            if (clamped) atomicOr(p.status, DFLASH_FLAG_PAGE_CLAMPED);
-            for (int u = vdone - kVRawStages < 0 ? 0 : vdone - kVRawStages; u < vdone; ++u)
-                mbar_wait(smem_u32(&sm.vfull[u % kVRawStages]), (u / kVRawStages) & 1, &sm.abort,
-                          kWaitLimitNs);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
@@ -411,17 +384,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (lane == 0) mma_commit(smem_u32(&sm.odone));  // tracks every MMA issued above
-    } else if (warp < 2 + kVWarps) {
-        // ---------------------------------------------------------------- V decode (2 warps)
-        const int vt = tid - 64;
-        for (int u = 0; u < nhalves; ++u) {
-            const int st3 = u % kVRawStages;
-            if (!ctx.wait_warp(&sm.vfull[st3], (u / kVRawStages) & 1)) break;
-            const uint8_t* raw = smem + kOffVRaw + st3 * kVRawStage;
+    } else if (warp == 2) {
+        // ------------------------------------------------- V copies (TMA): 64-key halves
+        if (lane == 0) {
+            bool clamped = false;
+            int vdone = 0;
+            for (int u = 0; u < nhalves; ++u) {
+                const int st = u % kVRawStages;
+                const int h0 = start + u * kHalf;
+                int rows[kHalf / kChunk];
+                int nval = 0;
+#pragma unroll
+                for (int c = 0; c < kHalf / kChunk; ++c) {
+                    const int j0 = h0 + kChunk * c;
+                    rows[c] = -1;
+                    if (j0 < end) {
+                        rows[c] = chunk_row(p, sm, b, start, j0, &clamped);
+                        ++nval;
+                    }
+                }
+                if (!ctx.wait(&sm.vfree[st], ((u / kVRawStages) & 1) ^ 1)) break;
+                mbar_arrive_expect_tx(smem_u32(&sm.vfull[st]), nval * kChunk * kHeadDim);
+                const uint32_t dst = smem_u32(smem + kOffVRaw + st * kVRawStage);
+#pragma unroll
+                for (int c = 0; c < kHalf / kChunk; ++c)
+                    if (rows[c] >= 0)
+                        tma_load_2d(dst + c * 4096, &vmap, h * kHeadDim, rows[c],
+                                    smem_u32(&sm.vfull[st]));
+                vdone = u + 1;
+            }
+            if (clamped) atomicOr(p.status, DFLASH_FLAG_PAGE_CLAMPED);
+            // no copy may still be writing shared memory when the CTA retires
+            for (int u = vdone - kVRawStages < 0 ? 0 : vdone - kVRawStages; u < vdone; ++u)
+                mbar_wait(smem_u32(&sm.vfull[u % kVRawStages]), (u / kVRawStages) & 1, &sm.abort,
+                          kWaitLimitNs);
+        }
+    } else if (warp >= kVWarp0) {
+        // ------------------------------------------------- V decode (warps 12-15)
+        // All four warps decode every 32-key stage together into a 2-deep FP16 ring that the PV
+        // MMAs consume in key order; a raw stage is released once all four have read it.
+        const int vt = tid - kVWarp0 * 32;
+        bool ok = true;
+        for (int u = 0; ok && u < nhalves; ++u) {
+            const int st = u % kVRawStages;
+            if (!ctx.wait_warp(&sm.vfull[st], (u / kVRawStages) & 1)) break;
+            const uint8_t* raw = smem + kOffVRaw + st * kVRawStage;
             const int h0 = start + u * kHalf;
-            bool ok = true;
 #pragma unroll 1
-            for (int q2 = 0; q2 < kHalf / kVhKeys; ++q2) {
+            for (int q2 = 0; ok && q2 < kHalf / kVhKeys; ++q2) {
                 const int e = 2 * u + q2;  // 32-key stage index
                 const int vs = e % kVhStages;
                 if (!ctx.wait_warp(&sm.vhempty[vs], ((e / kVhStages) & 1) ^ 1)) {
@@ -429,21 +439,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 uint8_t* vh = smem + kOffVh + vs * kVhStage;
-                uint4 w[8];
+                uint4 w[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int id = i * 64 + vt;
+                for (int i = 0; i < 4; ++i) {
+                    const int id = i * 128 + vt;
                     const int kk = q2 * kVhKeys + (id >> 4);  // key within the half
-                    const int cc = id & 15;                    // 16-byte chunk of the row
-                    // raw stage: two 128-byte-swizzled column halves of 64 rows each
-                    const uint32_t off = (cc >> 3) * (kVRawStage / 2) + kk * 128 +
-                                         ((((cc & 7) ^ (kk & 7))) << 4);
-                    w[i] = h0 + kk < end ? *reinterpret_cast<const uint4*>(raw + off)
+                    w[i] = h0 + kk < end ? *reinterpret_cast<const uint4*>(
+                                               raw + kk * kHeadDim + (id & 15) * 16)
                                          : make_uint4(0, 0, 0, 0);
                 }
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int id = i * 64 + vt;
+                for (int i = 0; i < 4; ++i) {
+                    const int id = i * 128 + vt;
                     const int key = id >> 4, c = id & 15;
                     uint4 f0, f1;
                     e4m3x4_to_f16x4(w[i].x, f0.x, f0.y);
@@ -458,10 +465,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(smem_u32(&sm.vhfull[vs]));
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sm.vfree[st3]));
-            if (!ok) break;
+            if (lane == 0) mbar_arrive(smem_u32(&sm.vfree[st]));
         }
-    } else {
+    } else if (warp >= 4) {
         // ---------------------------------------------------------------- softmax (2 groups)
         const int sw = warp - 4;          // 0..7
         const int wg = sw >> 2;           // rows [wg * RH, wg * RH + RH)
@@ -532,7 +538,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                               kmajor_off(term * RP + r, lane * 8, SN)) =
                         make_uint2(packed[0], packed[1]);
                 }
-                if (lane == 0) sm.c0[r] = qk_scale * __int_as_float((127 - a) << 23);
+                if (lane == 0) {
+                    sm.c0[r] = qk_scale * __int_as_float((127 - a) << 23);
+                    sm.negm[r] = INFINITY;  // no key seen yet
+                }
             }
             constexpr int kPadChunks = kTile * (kPN - RP) / 8;
             for (int i = tid - 128; i < kPStages * kPadChunks; i += 256) {
@@ -548,15 +557,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         int epoch = 0;
         bool alive = ctx.wait_warp(&sm.qready, 0);
-        float c0[RH], negm[RH], lsum[RH];
+        // per-row scale and minus reference max live in shared memory (read as float4 vectors,
+        // identical for every thread of the group); row sums stay in registers
+        float lsum[RH];
         uint32_t rowmask = 0;
 #pragma unroll
         for (int i = 0; i < RH; ++i) {
-            c0[i] = sm.c0[row0 + i];
-            negm[i] = INFINITY;  // minus the reference max; +inf: no key seen yet
             lsum[i] = 0.f;
             rowmask |= (uint32_t)(row0 + i < R) << i;
         }
+        const float4* c0v = reinterpret_cast<const float4*>(sm.c0 + row0);
+        float4* negmv = reinterpret_cast<float4*>(sm.negm + row0);
         for (int t = 0; alive && t < ntiles; ++t) {
             const int s = t & 1;
             const uint32_t ph = (t >> 1) & 1;
@@ -571,17 +582,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             // y = S0 + S1/16 + S2/256: the raw score in MMA units, kept in registers
             float y[RH];
             {
-                uint32_t a0[RH], a1[RH];
-                tmem_load_cols<RH>(sbase, a0);
-                tmem_load_cols<RH>(sbase + RP, a1);
-                tmem_ld_wait_n<RH>(a0);
-                tmem_ld_wait_n<RH>(a1);
+                uint32_t a[RH];
+                tmem_load_cols<RH>(sbase, a);
+                tmem_ld_wait_n<RH>(a);
 #pragma unroll
-                for (int i = 0; i < RH; ++i) y[i] = fmaf(f32(a1[i]), 0.0625f, f32(a0[i]));
-                tmem_load_cols<RH>(sbase + 2 * RP, a0);
-                tmem_ld_wait_n<RH>(a0);
+                for (int i = 0; i < RH; ++i) y[i] = f32(a[i]);
+                tmem_load_cols<RH>(sbase + RP, a);
+                tmem_ld_wait_n<RH>(a);
 #pragma unroll
-                for (int i = 0; i < RH; ++i) y[i] = fmaf(f32(a0[i]), 0.00390625f, y[i]);
+                for (int i = 0; i < RH; ++i) y[i] = fmaf(f32(a[i]), 0.0625f, y[i]);
+                tmem_load_cols<RH>(sbase + 2 * RP, a);
+                tmem_ld_wait_n<RH>(a);
+#pragma unroll
+                for (int i = 0; i < RH; ++i) y[i] = fmaf(f32(a[i]), 0.00390625f, y[i]);
             }
             tc_fence_before();
             __syncwarp();
@@ -594,11 +607,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!v) validm &= ~(1u << i);
                 }
             }
+            // y <- score in log2 units; does any visible score exceed its row's reference max by
+            // more than 2^8?
             bool need = false;
 #pragma unroll
-            for (int i = 0; i < RH; ++i) {
-                const float yi = fmaf(y[i], c0[i], negm[i]);
-                need |= ((validm >> i) & 1u) && yi > kLazyThreshold;
+            for (int i4 = 0; i4 < RH / 4; ++i4) {
+                const float4 c = c0v[i4], nm = negmv[i4];
+                y[4 * i4 + 0] *= c.x;
+                y[4 * i4 + 1] *= c.y;
+                y[4 * i4 + 2] *= c.z;
+                y[4 * i4 + 3] *= c.w;
+                need |= ((validm >> (4 * i4 + 0)) & 1u) && y[4 * i4 + 0] + nm.x > kLazyThreshold;
+                need |= ((validm >> (4 * i4 + 1)) & 1u) && y[4 * i4 + 1] + nm.y > kLazyThreshold;
+                need |= ((validm >> (4 * i4 + 2)) & 1u) && y[4 * i4 + 2] + nm.z > kLazyThreshold;
+                need |= ((validm >> (4 * i4 + 3)) & 1u) && y[4 * i4 + 3] + nm.w > kLazyThreshold;
             }
             bool need_any = false;
             if (!wg_sync(ctx, wg, wq, epoch, __any_sync(0xffffffffu, need), &need_any)) {
@@ -610,24 +632,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // exact tile maximum per row -> new reference max; rescale row sums and O
 #pragma unroll
                 for (int i = 0; i < RH; ++i) {
-                    const float x = ((validm >> i) & 1u) ? y[i] * c0[i] : -INFINITY;
-                    const float m = warp_max(x);
+                    const float m = warp_max(((validm >> i) & 1u) ? y[i] : -INFINITY);
                     if (lane == 0) sm.red[wg][wq][i] = m;
                 }
                 ok = wg_sync(ctx, wg, wq, epoch, false, nullptr);
+                float mnew_own = 0.f;
+                bool own = false;
                 if (ok) {
 #pragma unroll
                     for (int i = 0; i < RH; ++i) {
-                        const float mo = -negm[i];
+                        const float mo = -sm.negm[row0 + i];
                         const float tm = fmaxf(fmaxf(sm.red[wg][0][i], sm.red[wg][1][i]),
                                                fmaxf(sm.red[wg][2][i], sm.red[wg][3][i]));
                         const float mn = fmaxf(mo, tm);
                         const float alpha = (mn == -INFINITY) ? 1.f : ex2(mo - mn);
                         lsum[i] *= alpha;
-                        negm[i] = -mn;
-                        if (i == st) sm.alpha[row0 + i] = alpha;
+                        if (i == st) {
+                            sm.alpha[row0 + i] = alpha;
+                            mnew_own = mn;
+                            own = true;
+                        }
                     }
-                    ok = wg_sync(ctx, wg, wq, epoch, false, nullptr);  // alphas visible
+                    ok = wg_sync(ctx, wg, wq, epoch, false, nullptr);  // alphas visible, old m read
+                    if (own) sm.negm[row0 + st] = -mnew_own;
+                    ok = ok && wg_sync(ctx, wg, wq, epoch, false, nullptr);  // new m visible
                 }
                 if (ok && t > 0) {
                     // O holds tiles < t: wait for their PV, then scale this group's row columns
@@ -663,10 +691,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int q2 = 0; q2 < 4; ++q2) {
                     const int i0 = c * 8 + 2 * q2, i1 = i0 + 1;
-                    const float p0 =
-                        ((validm >> i0) & 1u) ? ex2(fmaf(y[i0], c0[i0], negm[i0])) : 0.f;
-                    const float p1 =
-                        ((validm >> i1) & 1u) ? ex2(fmaf(y[i1], c0[i1], negm[i1])) : 0.f;
+                    const float p0 = ((validm >> i0) & 1u) ? ex2(y[i0] + sm.negm[row0 + i0]) : 0.f;
+                    const float p1 = ((validm >> i1) & 1u) ? ex2(y[i1] + sm.negm[row0 + i1]) : 0.f;
                     lsum[i0] += p0;
                     lsum[i1] += p1;
                     const __half2 hp = __floats2half2_rn(p0, p1);
@@ -694,7 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (st == i && row0 + i < R) {
                     const float L = sm.red[wg][0][i] + sm.red[wg][1][i] + sm.red[wg][2][i] +
                                     sm.red[wg][3][i];
-                    p.ws_state[unit * R + row0 + i] = make_float2(-negm[i], L);
+                    p.ws_state[unit * R + row0 + i] = make_float2(-sm.negm[row0 + i], L);
                 }
             }
         }
@@ -775,7 +801,7 @@ cudaError_t launch_tc_partial(const PartialParams& p, cudaStream_t stream) {
                                 (cuuint64_t)p.num_pages * p.page_size};
     const cuuint64_t strides[1] = {(cuuint64_t)p.num_kv_heads * kHeadDim};
     const cuuint32_t kbox[2] = {128, tc::kChunk};
-    const cuuint32_t vbox[2] = {128, tc::kChunk};
+    const cuuint32_t vbox[2] = {kHeadDim, tc::kChunk};
     const cuuint32_t estride[2] = {1, 1};
     CUresult r1 = encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.k_pool),
                          dims, strides, kbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -783,7 +809,7 @@ cudaError_t launch_tc_partial(const PartialParams& p, cudaStream_t stream) {
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     CUresult r2 = encode(&vmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.v_pool),
                          dims, strides, vbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r1 != CUDA_SUCCESS || r2 != CUDA_SUCCESS) return cudaErrorInvalidValue;
     switch (rp) {

@@ -64,33 +64,41 @@ class LayerStack:
                                          lay["block_table"], lay["context_lens"], lay["k_scale"],
                                          lay["v_scale"], self.att.workspace, out, lse, stream)
 
-    def launch_timed(self, partial_events, combine_events, stream=None):
-        """Same launches, with CUDA events around every kernel (attribution pass)."""
-        for l, (lay, out, lse) in enumerate(zip(self.layers, self.outs, self.lses)):
-            partial_events[l][0].record()
+    def launch_partial(self, stream=None):
+        """Only the partial-attention kernels of the 16 layers."""
+        for lay in self.layers:
             B.dflash_verify_attn_run(self.plan, lay["q"], lay["k_pool"], lay["v_pool"],
                                      lay["block_table"], lay["context_lens"], lay["k_scale"],
                                      lay["v_scale"], self.att.workspace, stream)
-            partial_events[l][1].record()
-            combine_events[l][0].record()
+
+    def launch_combine(self, stream=None):
+        """Only the combine kernels of the 16 layers (re-reading the workspace state)."""
+        for lay, out, lse in zip(self.layers, self.outs, self.lses):
             B.dflash_verify_attn_combine(self.plan, self.att.workspace, lay["context_lens"], out,
                                          lse, stream)
-            combine_events[l][1].record()
 
-    def capture(self):
-        """Capture one 16-layer step into a CUDA graph (warm-up launch first)."""
+    def _capture(self, fn):
         s = torch.cuda.Stream(device=self.device)
         s.wait_stream(torch.cuda.current_stream(self.device))
         with torch.cuda.stream(s):
-            self.launch()
+            fn()
         torch.cuda.current_stream(self.device).wait_stream(s)
         torch.cuda.synchronize(self.device)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.launch()
+            fn()
         torch.cuda.synchronize(self.device)
-        self.graph = g
         return g
+
+    def capture(self):
+        """Capture one 16-layer step into a CUDA graph (warm-up launch first)."""
+        self.graph = self._capture(self.launch)
+        return self.graph
+
+    def capture_kernel_graphs(self):
+        """Graphs of the 16 partial kernels alone and of the 16 combine kernels alone, so that
+        each kernel's device time can be taken from CUDA events without host launch gaps."""
+        return self._capture(self.launch_partial), self._capture(self.launch_combine)
 
     def replay(self):
         self.graph.replay()
