@@ -166,6 +166,18 @@ def oracle_ms_per_step(w, layers_sample, rows_note, steps=1):
     return per_layer * w.layers * 1e3, orc.num_threads(), times
 
 
+def max_over_ranks(value, world, device):
+    """Largest value over the ranks of the process group (the job is as slow as its slowest
+    rank); works for NCCL (CUDA tensors) and gloo (CPU tensors)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_reference(args, rank, world):
     w = workload(args.config)
     if rank != 0:
@@ -244,11 +256,7 @@ def run_ours(args, rank, world, local_rank):
             ends[s].record()
         barrier()
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(step_ms), world, dev)
 
     # kernel attribution: the same 16 partial launches (and, separately, the 16 combine launches)
     # replayed from their own graphs, CUDA events around each replay on the replay stream
@@ -308,11 +316,7 @@ def run_ours(args, rank, world, local_rank):
             e2e_step()
             ev[s][1].record()
         barrier()
-        e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), world, dev)
         e2e = {"value": round(e2e_ms, 4), "unit": "ms", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
 
