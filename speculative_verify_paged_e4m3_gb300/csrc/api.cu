@@ -19,7 +19,8 @@ cudaError_t launch_simt_partial(const PartialParams& p, cudaStream_t stream);
 cudaError_t launch_tc_partial(const PartialParams& p, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 size_t simt_smem_bytes();
-size_t tc_smem_bytes();
+size_t tc_smem_bytes(int rows);
+int tc_threads(int rows);
 bool tc_supports(int rows);
 }  // namespace dflash
 
@@ -134,8 +135,8 @@ int dflash_verify_attn_plan(const dflash_verify_attn_problem* pr,
         plan->kernel = DFLASH_KERNEL_TCGEN05;
         plan->tile_keys = 128;
         plan->min_split_keys = 256;
-        plan->threads = 384;
-        plan->smem_bytes = (int32_t)tc_smem_bytes();
+        plan->threads = tc_threads((int)rows);
+        plan->smem_bytes = (int32_t)tc_smem_bytes((int)rows);
     } else {
         plan->kernel = DFLASH_KERNEL_SIMT;
         plan->tile_keys = 32;

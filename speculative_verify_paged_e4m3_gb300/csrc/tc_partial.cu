@@ -6,25 +6,31 @@
 // numerator ("complete FP32 workspace", "[Perf] Reduce DFlash2 attention cost and screen exact QK
 // reuse", Purpose). The GB300 design:
 //
-//  * keys on the MMA's M dimension (M = 128 keys per tile), query rows on N, so no MMA work is
-//    spent on padding rows: S^T = K Q^T and O^T = V^T P^T, both with M = 128.
-//  * QK^T runs on raw E4M3 K codes (kind::f8f6f4): K pages go from HBM to 128-byte-swizzled shared
-//    memory by TMA and straight into the tensor core, with no decode. Q (FP16) is split exactly
-//    into three E4M3 terms q * 2^a = t0 + t1/16 + t2/256 (per-row power-of-two a), stacked on N
-//    (N = 3 x rows), and the score is (S0 + S1/16 + S2/256) * 2^-a * k_scale / 16 * log2 e.
-//  * PV runs in FP16 (kind::f16): V codes are decoded exactly to FP16 with cvt.f16x2.e4m3x2 into
-//    MN-major 32-key stages, P (<= 2^8) is rounded to FP16 into an MN-major tile (N padded to 64),
-//    and O^T accumulates in tensor memory (FP32).
-//  * Softmax: keys on tensor-memory lanes (thread = key); two warpgroups split the query rows.
-//    Each keeps, per row, a reference max that only moves when a score exceeds it by more than 2^8
-//    (then the warpgroup rescales its O columns in tensor memory), and FP32 row sums of the
-//    unrounded probabilities, reduced across the key lanes once per split.
-//  * Warp roles: warp 0 copies K tiles (TMA, 2 stages); warp 1 owns tensor memory and issues the
-//    MMAs; warp 2 copies V in 64-key halves (TMA, 3 raw stages) and warps 2-3 decode them into
-//    32-key FP16 stages (2 deep); warps 4-11 stage the Q terms (while the first
-//    copies are in flight), then run the softmax (rows 0..RP/2-1 and RP/2..RP-1) and write O out.
-//    K and V copies come from two different warps: one issuing warp tops out well below the HBM
-//    rate on this GPU (measured), two reach it.
+//  * Both products run on the raw E4M3 cache codes (kind::f8f6f4), so no K or V byte is ever
+//    decoded or rewritten: K and V pages go from HBM into 128-byte-swizzled shared memory by TMA
+//    and straight into the tensor core. Keys sit on the MMA's M dimension (M = 128 keys per tile)
+//    and query rows on N: S^T = K Q^T (K K-major) and O^T = V^T P^T (V read MN-major from the very
+//    same tile layout), so no MMA work is spent on padding rows.
+//  * Q (FP16) is split exactly into three E4M3 terms q * 2^a = t0 + t1/16 + t2/256 (per-row
+//    power-of-two a), stacked on N (N = 3 x rows); the score is (S0 + S1/16 + S2/256) * 2^-a *
+//    k_scale / 16 * log2 e.
+//  * The probabilities, taken as p = 2^(s - m) * 2^score with s = 4 and a reference max m (so
+//    p <= 2^8, see below), are split the same way into three E4M3 terms p = h + m/16 + l/256
+//    (Veltkamp splitting in FP32, relative error about 2^-12, finer than an FP16 P), stacked on N,
+//    so O^T accumulates three FP32 terms that are summed at the end. The shift s keeps the leading
+//    term out of E4M3's subnormal range down to p = 2^-10 of the reference: below 2^-6 the
+//    leading term only has a 2^-9 grid, and over 10^5 keys those roundings add up.
+//  * Softmax: keys on tensor-memory lanes (thread = key); RP/16 warpgroups of 16 query rows each.
+//    Each keeps, per row, a reference max that only moves when a score exceeds it by more than
+//    2^(8 - s) (then the warpgroup rescales its O columns in tensor memory), and FP32 row sums of
+//    the unrounded (shifted) probabilities, reduced across the key lanes once per split. The
+//    split state keeps m - s as its max, which makes the shift invisible to the combine.
+//  * Warp roles: warp 0 copies K tiles (TMA, 2 stages of 128 keys); warp 1 owns tensor memory and
+//    issues the MMAs; warp 2 copies V (TMA, 64-key stages) and zeroes the keys past the context
+//    in the last one (a zero probability must not meet a NaN code); warps 4.. stage the Q terms
+//    (while the first copies are in flight), then run the softmax and write O out. K and V copies
+//    come from two different warps: one issuing warp tops out well below the HBM rate on this GPU
+//    (measured), two reach it.
 //    Every wait is bounded: on timeout the CTA sets DFLASH_FLAG_KERNEL_TIMEOUT, drains its copies
 //    and returns.
 #include <cuda.h>
@@ -44,56 +50,69 @@ namespace tc {
 
 using namespace ptx;
 
-constexpr int kTile = 128;   // keys per tile = MMA M
-constexpr int kChunk = 16;   // keys per TMA box (pages are multiples of 16 tokens)
-constexpr int kVhKeys = 32;  // keys per decoded-V stage (two MMA K steps)
-constexpr int kTerms = 3;    // E4M3 terms of Q
-constexpr int kMaxRP = 48;   // padded rows per KV head this kernel carries
-constexpr int kPN = 64;      // N of the PV MMA (rows padded to one 128-byte swizzle atom)
-constexpr int kThreads = 512;
-constexpr int kVWarps = 4;     // warps 12-15: V decode
-constexpr int kVWarp0 = 12;
-constexpr int kHalf = 64;      // keys per raw-V stage
-constexpr int kVRawStages = 3;
+constexpr int kTile = 128;    // keys per tile = MMA M
+constexpr int kChunk = 16;    // keys per TMA box (pages are multiples of 16 tokens)
+constexpr int kVKeys = 64;    // keys per V stage
+constexpr int kTerms = 3;     // E4M3 terms of Q and of P
+constexpr int kMaxRP = 48;    // padded rows per KV head this kernel carries
+constexpr int kGroupRows = 16;
+constexpr int kKStages = 2;
+constexpr int kVStages = 5;
 constexpr int kPStages = 2;
-constexpr int kVhStages = 2;
 
-constexpr uint32_t kQBytes = kTerms * kMaxRP * kHeadDim;  // 36864
-constexpr uint32_t kKStage = kTile * kHeadDim;            // 32768
-constexpr uint32_t kVRawStage = kHalf * kHeadDim;         // 16384
-constexpr uint32_t kVhStage = kVhKeys * kHeadDim * 2;     // 16384
-constexpr uint32_t kPStage = kPN * kTile * 2;             // 16384
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kQBytes;
-constexpr uint32_t kOffVRaw = kOffK + 2 * kKStage;
-constexpr uint32_t kOffVh = kOffVRaw + kVRawStages * kVRawStage;
-constexpr uint32_t kOffP = kOffVh + kVhStages * kVhStage;
-constexpr uint32_t kOffSmall = kOffP + kPStages * kPStage;
-
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kSStride = 192, kColO = 384, kOStride = 64;
+constexpr uint32_t kKStage = kTile * kHeadDim;   // 32768: two 128-byte column blocks of 128 keys
+constexpr uint32_t kVStage = kVKeys * kHeadDim;  // 16384: two 128-byte column blocks of 64 keys
+constexpr uint32_t kKHalf = kKStage / 2;
+constexpr uint32_t kVHalf = kVStage / 2;
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
 constexpr int kRowCache = 512;  // 16-key chunks of a split whose source row is looked up up front
-constexpr float kLazyThreshold = 8.f;
+constexpr float kPShift = 4.f;         // s: probabilities are scaled by 2^s before the split
+constexpr float kLazyThreshold = 8.f;  // largest shifted probability exponent, 8 - s above the max
+
+// Per-row-count layout. Shared memory: Q terms | K stages | V stages | P stages | Small.
+// Tensor memory: S^T (3 x RP columns) then O^T of the two head-dim halves (3 x RP columns each).
+template <int RP>
+struct Cfg {
+    static constexpr int kGroups = RP / kGroupRows;
+    static constexpr int kSoftWarps = 4 * kGroups;
+    static constexpr int kThreads = 128 + 32 * kSoftWarps;
+    static constexpr int SN = kTerms * RP;  // N of both MMAs
+    static constexpr uint32_t kQBytes = SN * kHeadDim;
+    static constexpr uint32_t kPStage = SN * kTile;
+    static constexpr uint32_t kOffQ = 0;
+    static constexpr uint32_t kOffK = kOffQ + kQBytes;
+    static constexpr uint32_t kOffV = kOffK + kKStages * kKStage;
+    static constexpr uint32_t kOffP = kOffV + kVStages * kVStage;
+    static constexpr uint32_t kOffSmall = kOffP + kPStages * kPStage;
+    static constexpr uint32_t kColS = 0, kColO = SN;
+    static constexpr uint32_t kTmemCols = 3 * SN <= 256 ? 256 : 512;
+    static_assert(RP % kGroupRows == 0 && RP <= kMaxRP, "rows per CTA");
+    static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0, "swizzled stages need 1 KB alignment");
+    static_assert(kOffSmall % 16 == 0, "Small must start 16-byte aligned");
+    static_assert(3 * SN <= 512, "tensor memory budget");
+};
 
 struct Small {
-    uint64_t kfull[2], kempty[2], sfull[2], sempty[2], pfull[kPStages], pempty[kPStages];
-    uint64_t vfull[kVRawStages], vfree[kVRawStages], vhfull[kVhStages], vhempty[kVhStages];
+    uint64_t kfull[kKStages], kempty[kKStages], sfull, sempty, pfull[kPStages], pempty[kPStages];
+    uint64_t vfull[kVStages], vfree[kVStages], vtail;
     uint64_t odone, qready;
     uint32_t tmem_base;
     int abort;
-    int flag[2][2][4];            // softmax group barrier: [group][epoch parity][warp]
-    alignas(16) float c0[kMaxRP];    // score scale of each row (log2 units per MMA unit), read as float4
-    alignas(16) float negm[kMaxRP];  // minus the reference max of each row (+inf: no key yet), float4
-    float red[2][4][kMaxRP / 2];  // per-warpgroup, per-warp partials (tile max, row sums)
+    int flag[kMaxRP / kGroupRows][2][4];  // group barrier: [group][epoch parity][warp]
+    alignas(16) float c0[kMaxRP];    // score scale of each row (log2 units per MMA unit), float4 reads
+    alignas(16) float negm[kMaxRP];  // s minus the reference max of each row (+inf: none yet), float4
+    float red[kMaxRP / kGroupRows][4][kGroupRows];  // per-group, per-warp partials (max, row sums)
     float alpha[kMaxRP];
-    int rows[kRowCache];          // source row (physical page * page + slot) of chunk c of the split
+    int rows[kRowCache];  // source row (physical page * page + slot) of chunk c of the split
 };
-constexpr uint32_t kSmemBytes = kOffSmall + sizeof(Small);
 static_assert(offsetof(Small, c0) % 16 == 0 && offsetof(Small, negm) % 16 == 0,
               "row constants are read as float4");
-static_assert(kOffSmall % 16 == 0, "Small must start 16-byte aligned");
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+template <int RP>
+constexpr uint32_t smem_bytes() {
+    return Cfg<RP>::kOffSmall + sizeof(Small);
+}
+static_assert(smem_bytes<kMaxRP>() <= 227 * 1024, "shared memory budget");
 
 // Byte offset of (row, byte k along K) in a K-major, 128-byte-swizzled operand with `rows` rows
 // (8-row groups 1 KB apart, 128-byte K columns rows*128 bytes apart).
@@ -103,11 +122,12 @@ __device__ __forceinline__ uint32_t kmajor_off(int row, int kbyte, int rows) {
            ((((w >> 4) ^ (row & 7)) << 4) | (w & 15));
 }
 
-// Byte offset of the 16-byte chunk holding FP16 elements (mn .. mn+7, k) of an MN-major,
-// 128-byte-swizzled operand: 64-element MN atoms `atom_stride` bytes apart, 8-k groups 1 KB apart.
-__device__ __forceinline__ uint32_t mnmajor_chunk(int mn, int k, uint32_t atom_stride) {
-    const int e = mn & 63, kr = k & 7;
-    return (mn >> 6) * atom_stride + (k >> 3) * 1024 + kr * 128 + ((((e >> 3) ^ kr)) << 4);
+// P stage: an MN-major, unswizzled 8-bit operand of N = 3*RP rows by 128 keys, made of 16-row x
+// 8-key core matrices (128 bytes, key-major inside): key groups 128 bytes apart (the descriptor's
+// leading offset), 16-row blocks 2 KB apart (its stride offset). Byte offset of the 16 rows
+// [16*nb, 16*nb + 16) of key k.
+__device__ __forceinline__ uint32_t p_chunk(int nb, int k) {
+    return nb * 2048 + (k >> 3) * 128 + (k & 7) * 16;
 }
 
 __device__ __forceinline__ float f32(uint32_t x) { return __uint_as_float(x); }
@@ -121,6 +141,24 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+// Split two probabilities (0 <= x <= 2^8) into three E4M3 terms x = h + m/16 + l/256 and return
+// the codes, two per 16-bit word (first value in the low byte). h and m are x and the scaled
+// residual rounded to 4 significant bits by Veltkamp splitting (c = x(2^20 + 1), h = c - (c - x),
+// exact in FP32 with round-to-nearest), so both are E4M3 values whenever they are at least 2^-6
+// and the residuals are exact; l is the last residual rounded to nearest by the conversion.
+__device__ __forceinline__ void split3_x2(float a, float b, uint32_t& h, uint32_t& m, uint32_t& l) {
+    constexpr float kC = 1048577.f;  // 2^20 + 1
+    const float ca = __fmul_rn(a, kC), cb = __fmul_rn(b, kC);
+    const float ha = __fsub_rn(ca, __fsub_rn(ca, a)), hb = __fsub_rn(cb, __fsub_rn(cb, b));
+    const float ra = __fmul_rn(__fsub_rn(a, ha), 16.f), rb = __fmul_rn(__fsub_rn(b, hb), 16.f);
+    const float da = __fmul_rn(ra, kC), db = __fmul_rn(rb, kC);
+    const float ma = __fsub_rn(da, __fsub_rn(da, ra)), mb = __fsub_rn(db, __fsub_rn(db, rb));
+    const float la = __fmul_rn(__fsub_rn(ra, ma), 16.f), lb = __fmul_rn(__fsub_rn(rb, mb), 16.f);
+    h = f32x2_to_e4m3x2(ha, hb);
+    m = f32x2_to_e4m3x2(ma, mb);
+    l = f32x2_to_e4m3x2(la, lb);
 }
 
 struct Ctx {
@@ -186,34 +224,33 @@ __device__ __forceinline__ int chunk_row(const PartialParams& p, const Small& sm
     return phys * p.page_size + (j0 % p.page_size);
 }
 
-// Loads / stores of N consecutive 32-bit tensor-memory columns of this thread's lane (N = 8k).
-template <int N>
-__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* r) {
-    if constexpr (N >= 16) {
-        tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(r));
-        if constexpr (N > 16) tmem_load_cols<N - 16>(taddr + 16, r + 16);
-    } else if constexpr (N == 8) {
-        tmem_ld8(taddr, r);
-    }
-}
-template <int N>
-__device__ __forceinline__ void tmem_store_cols(uint32_t taddr, const uint32_t* r) {
-    if constexpr (N >= 16) {
-        tmem_st16(taddr, *reinterpret_cast<const uint32_t(*)[16]>(r));
-        if constexpr (N > 16) tmem_store_cols<N - 16>(taddr + 16, r + 16);
-    } else if constexpr (N == 8) {
-        tmem_st8(taddr, r);
-    }
+// The three term slices (columns base, base + RP, base + 2RP) of this lane's 16 rows, combined
+// as t0 + t1/16 + t2/256.
+template <int RP>
+__device__ __forceinline__ void load_terms16(uint32_t taddr, float (&y)[kGroupRows]) {
+    uint32_t a[16];
+    tmem_ld16(taddr, a);
+    tmem_ld_wait(a);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) y[i] = f32(a[i]);
+    tmem_ld16(taddr + RP, a);
+    tmem_ld_wait(a);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) y[i] = fmaf(f32(a[i]), 0.0625f, y[i]);
+    tmem_ld16(taddr + 2 * RP, a);
+    tmem_ld_wait(a);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) y[i] = fmaf(f32(a[i]), 0.00390625f, y[i]);
 }
 
 template <int RP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     tc_partial_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const PartialParams p) {
+    using C = Cfg<RP>;
     extern __shared__ __align__(1024) uint8_t smem[];
-    Small& sm = *reinterpret_cast<Small*>(smem + kOffSmall);
-    constexpr int SN = kTerms * RP;
-    constexpr int RH = RP / 2;  // rows per softmax warpgroup
+    Small& sm = *reinterpret_cast<Small*>(smem + C::kOffSmall);
+    constexpr int SN = C::SN;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int R = p.rows, G = p.group, P = p.page_size;
@@ -229,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (start >= n) return;  // idle split: the combine never reads it
     const int end = min(n, start + per);
     const int ntiles = (end - start + kTile - 1) / kTile;
-    const int nhalves = (end - start + kHalf - 1) / kHalf;
+    const int nvst = (end - start + kVKeys - 1) / kVKeys;
     if (smem_u32(smem) & 1023u) {  // the swizzled layouts need a 1 KB aligned base
         if (tid == 0) atomicOr(p.status, DFLASH_FLAG_KERNEL_TIMEOUT);
         return;
@@ -239,39 +276,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- set-up: barriers and tensor memory (Q terms are staged by the softmax warps while the
     // first copies are already in flight) ------------------------------------------------------
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kKStages; ++i) {
             mbar_init(smem_u32(&sm.kfull[i]), 1);
             mbar_init(smem_u32(&sm.kempty[i]), 1);
-            mbar_init(smem_u32(&sm.sfull[i]), 1);
-            mbar_init(smem_u32(&sm.sempty[i]), 8);
         }
+        mbar_init(smem_u32(&sm.sfull), 1);
+        mbar_init(smem_u32(&sm.sempty), C::kSoftWarps);
         for (int i = 0; i < kPStages; ++i) {
-            mbar_init(smem_u32(&sm.pfull[i]), 8);
+            mbar_init(smem_u32(&sm.pfull[i]), C::kSoftWarps);
             mbar_init(smem_u32(&sm.pempty[i]), 1);
         }
-        for (int i = 0; i < kVRawStages; ++i) {
+        for (int i = 0; i < kVStages; ++i) {
             mbar_init(smem_u32(&sm.vfull[i]), 1);
-            mbar_init(smem_u32(&sm.vfree[i]), kVWarps);
+            mbar_init(smem_u32(&sm.vfree[i]), 1);
         }
-        for (int i = 0; i < kVhStages; ++i) {
-            mbar_init(smem_u32(&sm.vhfull[i]), kVWarps);
-            mbar_init(smem_u32(&sm.vhempty[i]), 1);
-        }
+        mbar_init(smem_u32(&sm.vtail), 1);
         mbar_init(smem_u32(&sm.odone), 1);
-        mbar_init(smem_u32(&sm.qready), 8);
+        mbar_init(smem_u32(&sm.qready), C::kSoftWarps);
         sm.abort = 0;
-        for (int i = 0; i < 16; ++i) (&sm.flag[0][0][0])[i] = 0;
+        for (int i = 0; i < (int)(sizeof(sm.flag) / sizeof(int)); ++i) (&sm.flag[0][0][0])[i] = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
+        tmem_alloc(smem_u32(&sm.tmem_base), C::kTmemCols);
         tmem_relinquish();
     }
     {
         // block-table lookups of the split's chunks, all in flight at once
         bool clamped = false;
         const int nchunks = min((end - start + kChunk - 1) / kChunk, kRowCache);
-        for (int c = tid; c < nchunks; c += kThreads) {
+        for (int c = tid; c < nchunks; c += C::kThreads) {
             const int j0 = start + c * kChunk;
             const int phys = physical_page(p.block_table, b, p.max_pages_per_seq, j0 / P,
                                            p.num_pages, &clamped);
@@ -290,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool clamped = false;
             int kdone = 0;
             for (int t = 0; t < ntiles; ++t) {
-                const int s = t & 1;
+                const int s = t % kKStages;
                 const int tile0 = start + t * kTile;
                 int rows[kTile / kChunk];
                 int nval = 0;
@@ -303,76 +337,78 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ++nval;
                     }
                 }
-                if (!ctx.wait(&sm.kempty[s], ((t >> 1) & 1) ^ 1)) break;
+                if (!ctx.wait(&sm.kempty[s], ((t / kKStages) & 1) ^ 1)) break;
                 mbar_arrive_expect_tx(smem_u32(&sm.kfull[s]), nval * kChunk * kHeadDim);
-                const uint32_t dst = smem_u32(smem + kOffK + s * kKStage);
+                const uint32_t dst = smem_u32(smem + C::kOffK + s * kKStage);
 #pragma unroll
                 for (int c = 0; c < kTile / kChunk; ++c) {
                     if (rows[c] < 0) continue;
                     tma_load_2d(dst + c * 2048, &kmap, h * kHeadDim, rows[c],
                                 smem_u32(&sm.kfull[s]));
-                    tma_load_2d(dst + c * 2048 + kKStage / 2, &kmap, h * kHeadDim + 128, rows[c],
+                    tma_load_2d(dst + c * 2048 + kKHalf, &kmap, h * kHeadDim + 128, rows[c],
                                 smem_u32(&sm.kfull[s]));
                 }
                 kdone = t + 1;
             }
             if (clamped) atomicOr(p.status, DFLASH_FLAG_PAGE_CLAMPED);
             // no copy may still be writing shared memory when the CTA retires
-            for (int t = kdone - 2 < 0 ? 0 : kdone - 2; t < kdone; ++t)
-                mbar_wait(smem_u32(&sm.kfull[t & 1]), (t >> 1) & 1, &sm.abort, kWaitLimitNs);
+            for (int t = kdone - kKStages < 0 ? 0 : kdone - kKStages; t < kdone; ++t)
+                mbar_wait(smem_u32(&sm.kfull[t % kKStages]), (t / kKStages) & 1, &sm.abort,
+                          kWaitLimitNs);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0 && ctx.wait(&sm.qready, 0)) {
             const uint32_t idesc_qk = idesc_f32acc(128, SN, 0, 0, 0, 0);
-            const uint32_t idesc_pv = idesc_f32acc(128, kPN, 0, 0, 1, 1);
-            const uint32_t q_base = smem_u32(smem + kOffQ);
-            auto issue_qk = [&](int u) -> bool {
-                const int s = u & 1;
-                const uint32_t ph = (u >> 1) & 1;
-                if (!ctx.wait(&sm.kfull[s], ph)) return false;
-                if (!ctx.wait(&sm.sempty[s], ph ^ 1)) return false;
+            const uint32_t idesc_pv = idesc_f32acc(128, SN, 0, 0, 1, 1);
+            const uint32_t q_base = smem_u32(smem + C::kOffQ);
+            // S^T = K Q^T for tile t into the single S buffer (free once the softmax has read
+            // tile t-1's scores)
+            auto issue_qk = [&](int t) -> bool {
+                const int s = t % kKStages;
+                if (!ctx.wait(&sm.kfull[s], (t / kKStages) & 1)) return false;
+                if (!ctx.wait(&sm.sempty, (t & 1) ^ 1)) return false;
                 tc_fence_after();
-                const uint32_t kb = smem_u32(smem + kOffK + s * kKStage);
+                const uint32_t kb = smem_u32(smem + C::kOffK + s * kKStage);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t ad =
-                        smem_desc(kb + (kk >> 2) * (kKStage / 2) + (kk & 3) * 32, 16, 1024,
-                                  kSwizzle128B);
+                        smem_desc(kb + (kk >> 2) * kKHalf + (kk & 3) * 32, 16, 1024, kSwizzle128B);
                     const uint64_t bd = smem_desc(q_base + (kk >> 2) * (SN * 128) + (kk & 3) * 32,
                                                   16, 1024, kSwizzle128B);
-                    mma_f8_ss(tmem + kColS + s * kSStride, ad, bd, idesc_qk, kk > 0);
+                    mma_f8_ss(tmem + C::kColS, ad, bd, idesc_qk, kk > 0);
                 }
                 mma_commit(smem_u32(&sm.kempty[s]));
-                mma_commit(smem_u32(&sm.sfull[s]));
+                mma_commit(smem_u32(&sm.sfull));
                 return true;
             };
+            // O^T += V^T P^T for tile t: two V stages of 64 keys, two 32-key steps each, both
+            // head-dim halves
             auto issue_pv = [&](int t) -> bool {
                 const int pb = t % kPStages;
                 if (!ctx.wait(&sm.pfull[pb], (t / kPStages) & 1)) return false;
                 tc_fence_after();
-                const uint32_t pbase = smem_u32(smem + kOffP + pb * kPStage);
-                const int halves = min(2, nhalves - 2 * t);
+                const uint32_t pbase = smem_u32(smem + C::kOffP + pb * C::kPStage);
 #pragma unroll 1
-                for (int qq = 0; qq < 2 * halves; ++qq) {
-                    const int e = 4 * t + qq;  // 32-key stage index
-                    const int vs = e % kVhStages;
-                    if (!ctx.wait(&sm.vhfull[vs], (e / kVhStages) & 1)) return false;
+                for (int hv = 0; hv < kTile / kVKeys; ++hv) {
+                    const int u = (kTile / kVKeys) * t + hv;
+                    if (u >= nvst) break;
+                    const int vs = u % kVStages;
+                    if (!ctx.wait(&sm.vfull[vs], (u / kVStages) & 1)) return false;
                     tc_fence_after();
-                    const uint32_t vb = smem_u32(smem + kOffVh + vs * kVhStage);
+                    const uint32_t vb = smem_u32(smem + C::kOffV + vs * kVStage);
 #pragma unroll
-                    for (int ks = 0; ks < 2; ++ks) {
-                        const uint64_t bd = smem_desc(pbase + (4 * qq + 2 * ks) * 1024, kPStage,
-                                                      1024, kSwizzle128B);
+                    for (int kq = 0; kq < kVKeys / 32; ++kq) {
+                        const int kk = (kVKeys / 32) * hv + kq;  // 32-key step within the tile
+                        const uint64_t bd = smem_desc(pbase + kk * 512, 128, 2048, kSwizzleNone);
 #pragma unroll
                         for (int dh = 0; dh < 2; ++dh) {
-                            const uint64_t ad = smem_desc(vb + dh * 2 * 4096 + ks * 2048, 4096,
+                            const uint64_t ad = smem_desc(vb + dh * kVHalf + kq * 4096, kVHalf,
                                                           1024, kSwizzle128B);
-                            mma_f16_ss(tmem + kColO + dh * kOStride, ad, bd, idesc_pv,
-                                       (t | qq | ks) != 0);
+                            mma_f8_ss(tmem + C::kColO + dh * SN, ad, bd, idesc_pv, (t | kk) != 0);
                         }
                     }
-                    mma_commit(smem_u32(&sm.vhempty[vs]));
+                    mma_commit(smem_u32(&sm.vfree[vs]));
                 }
                 mma_commit(smem_u32(&sm.pempty[pb]));
                 return true;
@@ -385,17 +421,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) mma_commit(smem_u32(&sm.odone));  // tracks every MMA issued above
     } else if (warp == 2) {
-        // ------------------------------------------------- V copies (TMA): 64-key halves
-        if (lane == 0) {
-            bool clamped = false;
-            int vdone = 0;
-            for (int u = 0; u < nhalves; ++u) {
-                const int st = u % kVRawStages;
-                const int h0 = start + u * kHalf;
-                int rows[kHalf / kChunk];
+        // ------------------------------------------- V copies (TMA): 64-key stages, whole warp
+        bool clamped = false;
+        int vdone = 0;
+        bool tail_pending = false;  // the ragged last stage's copies are issued but not awaited
+        for (int u = 0; u < nvst; ++u) {
+            const int vs = u % kVStages;
+            const int h0 = start + u * kVKeys;
+            const int nkeys = min(kVKeys, end - h0);
+            const bool tail = nkeys < kVKeys;
+            if (!ctx.wait_warp(&sm.vfree[vs], ((u / kVStages) & 1) ^ 1)) break;
+            uint8_t* vstage = smem + C::kOffV + vs * kVStage;
+            const uint32_t bar = smem_u32(tail ? &sm.vtail : &sm.vfull[vs]);
+            if (lane == 0) {
+                int rows[kVKeys / kChunk];
                 int nval = 0;
 #pragma unroll
-                for (int c = 0; c < kHalf / kChunk; ++c) {
+                for (int c = 0; c < kVKeys / kChunk; ++c) {
                     const int j0 = h0 + kChunk * c;
                     rows[c] = -1;
                     if (j0 < end) {
@@ -403,97 +445,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ++nval;
                     }
                 }
-                if (!ctx.wait(&sm.vfree[st], ((u / kVRawStages) & 1) ^ 1)) break;
-                mbar_arrive_expect_tx(smem_u32(&sm.vfull[st]), nval * kChunk * kHeadDim);
-                const uint32_t dst = smem_u32(smem + kOffVRaw + st * kVRawStage);
+                mbar_arrive_expect_tx(bar, nval * kChunk * kHeadDim);
+                const uint32_t dst = smem_u32(vstage);
 #pragma unroll
-                for (int c = 0; c < kHalf / kChunk; ++c)
-                    if (rows[c] >= 0)
-                        tma_load_2d(dst + c * 4096, &vmap, h * kHeadDim, rows[c],
-                                    smem_u32(&sm.vfull[st]));
-                vdone = u + 1;
+                for (int c = 0; c < kVKeys / kChunk; ++c) {
+                    if (rows[c] < 0) continue;
+                    tma_load_2d(dst + c * 2048, &vmap, h * kHeadDim, rows[c], bar);
+                    tma_load_2d(dst + c * 2048 + kVHalf, &vmap, h * kHeadDim + 128, rows[c], bar);
+                }
             }
-            if (clamped) atomicOr(p.status, DFLASH_FLAG_PAGE_CLAMPED);
-            // no copy may still be writing shared memory when the CTA retires
-            for (int u = vdone - kVRawStages < 0 ? 0 : vdone - kVRawStages; u < vdone; ++u)
-                mbar_wait(smem_u32(&sm.vfull[u % kVRawStages]), (u / kVRawStages) & 1, &sm.abort,
-                          kWaitLimitNs);
-        }
-    } else if (warp >= kVWarp0) {
-        // ------------------------------------------------- V decode (warps 12-15)
-        // All four warps decode every 32-key stage together into a 2-deep FP16 ring that the PV
-        // MMAs consume in key order; a raw stage is released once all four have read it.
-        const int vt = tid - kVWarp0 * 32;
-        bool ok = true;
-        for (int u = 0; ok && u < nhalves; ++u) {
-            const int st = u % kVRawStages;
-            if (!ctx.wait_warp(&sm.vfull[st], (u / kVRawStages) & 1)) break;
-            const uint8_t* raw = smem + kOffVRaw + st * kVRawStage;
-            const int h0 = start + u * kHalf;
-#pragma unroll 1
-            for (int q2 = 0; ok && q2 < kHalf / kVhKeys; ++q2) {
-                const int e = 2 * u + q2;  // 32-key stage index
-                const int vs = e % kVhStages;
-                if (!ctx.wait_warp(&sm.vhempty[vs], ((e / kVhStages) & 1) ^ 1)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t* vh = smem + kOffVh + vs * kVhStage;
-                uint4 w[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int id = i * 128 + vt;
-                    const int kk = q2 * kVhKeys + (id >> 4);  // key within the half
-                    w[i] = h0 + kk < end ? *reinterpret_cast<const uint4*>(
-                                               raw + kk * kHeadDim + (id & 15) * 16)
-                                         : make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int id = i * 128 + vt;
-                    const int key = id >> 4, c = id & 15;
-                    uint4 f0, f1;
-                    e4m3x4_to_f16x4(w[i].x, f0.x, f0.y);
-                    e4m3x4_to_f16x4(w[i].y, f0.z, f0.w);
-                    e4m3x4_to_f16x4(w[i].z, f1.x, f1.y);
-                    e4m3x4_to_f16x4(w[i].w, f1.z, f1.w);
-                    *reinterpret_cast<uint4*>(vh + mnmajor_chunk(c * 16, key, 4096)) = f0;
-                    *reinterpret_cast<uint4*>(vh + mnmajor_chunk(c * 16 + 8, key, 4096)) = f1;
+            vdone = u + 1;
+            if (tail) {
+                // keys nkeys..63 of this stage (page-tail slots or never-copied rows) are zeroed
+                // once the copies have landed; a key's 128 bytes per half are contiguous
+                tail_pending = true;
+                if (!ctx.wait_warp(&sm.vtail, 0)) break;
+                tail_pending = false;
+                const int zero_chunks = (kVKeys - nkeys) * 8;  // 16-byte chunks per half
+                for (int i = lane; i < 2 * zero_chunks; i += 32) {
+                    const int dh = i / zero_chunks, c = i % zero_chunks;
+                    *reinterpret_cast<uint4*>(vstage + dh * kVHalf + nkeys * 128 + c * 16) =
+                        make_uint4(0, 0, 0, 0);
                 }
                 fence_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sm.vhfull[vs]));
+                if (lane == 0) mbar_arrive(smem_u32(&sm.vfull[vs]));
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sm.vfree[st]));
+        }
+        if (lane == 0) {
+            if (clamped) atomicOr(p.status, DFLASH_FLAG_PAGE_CLAMPED);
+            // no copy may still be writing shared memory when the CTA retires
+            for (int u = vdone - kVStages < 0 ? 0 : vdone - kVStages; u < vdone; ++u) {
+                const bool is_tail = end - (start + u * kVKeys) < kVKeys;
+                if (is_tail) {
+                    if (tail_pending) mbar_wait(smem_u32(&sm.vtail), 0, &sm.abort, kWaitLimitNs);
+                } else {
+                    mbar_wait(smem_u32(&sm.vfull[u % kVStages]), (u / kVStages) & 1, &sm.abort,
+                              kWaitLimitNs);
+                }
+            }
         }
     } else if (warp >= 4) {
-        // ---------------------------------------------------------------- softmax (2 groups)
-        const int sw = warp - 4;          // 0..7
-        const int wg = sw >> 2;           // rows [wg * RH, wg * RH + RH)
+        // ------------------------------------------------------------- softmax (RP/16 groups)
+        const int sw = warp - 4;          // 0 .. kSoftWarps - 1
+        const int g = sw >> 2;            // rows [16 g, 16 g + 16)
         const int wq = warp & 3;          // tensor-memory lane quadrant
         const int st = (wq << 5) | lane;  // key of the tile = tensor-memory lane
-        const int row0 = wg * RH;
+        const int row0 = kGroupRows * g;
         const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
         const int qoff = n - p.q_len;  // row r sees keys j <= qoff + r / G
 
-        // Q -> three E4M3 terms (one warp per row), row scales, zero P padding rows
+        // Q -> three E4M3 terms (one warp per row), row scales
         {
+            constexpr int kRowsPerWarp = RP / C::kSoftWarps;  // 4
             const float qk_scale = __ldg(p.k_scale) * 0.0625f * kLog2e;  // D^-1/2 = 1/16
-            uint4 qraw[RP / 8];  // this warp's rows sw, sw + 8, ...: all loads in flight at once
+            uint4 qraw[kRowsPerWarp];  // this warp's rows: all loads in flight at once
 #pragma unroll
-            for (int k = 0; k < RP / 8; ++k) {
-                const int r = sw + 8 * k;
+            for (int k = 0; k < kRowsPerWarp; ++k) {
+                const int r = sw + C::kSoftWarps * k;
                 qraw[k] = make_uint4(0, 0, 0, 0);
                 if (r < R) {
-                    const int i = r / G, g = r % G;
-                    const int64_t qrow = ((int64_t)b * p.q_len + i) * p.num_q_heads + h * G + g;
+                    const int i = r / G, gg = r % G;
+                    const int64_t qrow = ((int64_t)b * p.q_len + i) * p.num_q_heads + h * G + gg;
                     qraw[k] = *reinterpret_cast<const uint4*>(p.q + qrow * kHeadDim + lane * 8);
                 }
             }
 #pragma unroll
-            for (int k = 0; k < RP / 8; ++k) {
-                const int r = sw + 8 * k;
+            for (int k = 0; k < kRowsPerWarp; ++k) {
+                const int r = sw + C::kSoftWarps * k;
                 float qv[8];
                 const __half2* hh = reinterpret_cast<const __half2*>(&qraw[k]);
 #pragma unroll
@@ -534,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         qv[4 * w + 2] = (qv[4 * w + 2] - d23.x) * 16.f;
                         qv[4 * w + 3] = (qv[4 * w + 3] - d23.y) * 16.f;
                     }
-                    *reinterpret_cast<uint2*>(smem + kOffQ +
+                    *reinterpret_cast<uint2*>(smem + C::kOffQ +
                                               kmajor_off(term * RP + r, lane * 8, SN)) =
                         make_uint2(packed[0], packed[1]);
                 }
@@ -542,14 +561,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sm.c0[r] = qk_scale * __int_as_float((127 - a) << 23);
                     sm.negm[r] = INFINITY;  // no key seen yet
                 }
-            }
-            constexpr int kPadChunks = kTile * (kPN - RP) / 8;
-            for (int i = tid - 128; i < kPStages * kPadChunks; i += 256) {
-                const int stage = i / kPadChunks, rem = i % kPadChunks;
-                const int key = rem % kTile, c = RP / 8 + rem / kTile;
-                *reinterpret_cast<uint4*>(smem + kOffP + stage * kPStage +
-                                          mnmajor_chunk(c * 8, key, kPStage)) =
-                    make_uint4(0, 0, 0, 0);
             }
             fence_async_smem();
             __syncwarp();
@@ -559,59 +570,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool alive = ctx.wait_warp(&sm.qready, 0);
         // per-row scale and minus reference max live in shared memory (read as float4 vectors,
         // identical for every thread of the group); row sums stay in registers
-        float lsum[RH];
+        float lsum[kGroupRows];
         uint32_t rowmask = 0;
 #pragma unroll
-        for (int i = 0; i < RH; ++i) {
+        for (int i = 0; i < kGroupRows; ++i) {
             lsum[i] = 0.f;
             rowmask |= (uint32_t)(row0 + i < R) << i;
         }
         const float4* c0v = reinterpret_cast<const float4*>(sm.c0 + row0);
-        float4* negmv = reinterpret_cast<float4*>(sm.negm + row0);
+        const float4* negmv = reinterpret_cast<const float4*>(sm.negm + row0);
         for (int t = 0; alive && t < ntiles; ++t) {
-            const int s = t & 1;
-            const uint32_t ph = (t >> 1) & 1;
             const int tile0 = start + t * kTile;
             const int j = tile0 + st;
-            if (!ctx.wait_warp(&sm.sfull[s], ph)) {
+            if (!ctx.wait_warp(&sm.sfull, t & 1)) {
                 alive = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t sbase = lane_base + kColS + s * kSStride + row0;
             // y = S0 + S1/16 + S2/256: the raw score in MMA units, kept in registers
-            float y[RH];
-            {
-                uint32_t a[RH];
-                tmem_load_cols<RH>(sbase, a);
-                tmem_ld_wait_n<RH>(a);
-#pragma unroll
-                for (int i = 0; i < RH; ++i) y[i] = f32(a[i]);
-                tmem_load_cols<RH>(sbase + RP, a);
-                tmem_ld_wait_n<RH>(a);
-#pragma unroll
-                for (int i = 0; i < RH; ++i) y[i] = fmaf(f32(a[i]), 0.0625f, y[i]);
-                tmem_load_cols<RH>(sbase + 2 * RP, a);
-                tmem_ld_wait_n<RH>(a);
-#pragma unroll
-                for (int i = 0; i < RH; ++i) y[i] = fmaf(f32(a[i]), 0.00390625f, y[i]);
-            }
+            float y[kGroupRows];
+            load_terms16<RP>(lane_base + C::kColS + row0, y);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sm.sempty[s]));  // S buffer free for QK(t+2)
+            if (lane == 0) mbar_arrive(smem_u32(&sm.sempty));  // S free for QK(t+1)
             uint32_t validm = rowmask;  // bit i: key j visible to row row0 + i
             if (!((tile0 + kTile <= end) && (tile0 + kTile - 1 <= qoff))) {
 #pragma unroll
-                for (int i = 0; i < RH; ++i) {
+                for (int i = 0; i < kGroupRows; ++i) {
                     const bool v = j < end && j <= qoff + (row0 + i) / G;
                     if (!v) validm &= ~(1u << i);
                 }
             }
-            // y <- score in log2 units; does any visible score exceed its row's reference max by
-            // more than 2^8?
+            // y <- score in log2 units; would any visible shifted probability 2^(y + negm) exceed
+            // 2^8?
             bool need = false;
 #pragma unroll
-            for (int i4 = 0; i4 < RH / 4; ++i4) {
+            for (int i4 = 0; i4 < kGroupRows / 4; ++i4) {
                 const float4 c = c0v[i4], nm = negmv[i4];
                 y[4 * i4 + 0] *= c.x;
                 y[4 * i4 + 1] *= c.y;
@@ -623,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 need |= ((validm >> (4 * i4 + 3)) & 1u) && y[4 * i4 + 3] + nm.w > kLazyThreshold;
             }
             bool need_any = false;
-            if (!wg_sync(ctx, wg, wq, epoch, __any_sync(0xffffffffu, need), &need_any)) {
+            if (!wg_sync(ctx, g, wq, epoch, __any_sync(0xffffffffu, need), &need_any)) {
                 alive = false;
                 break;
             }
@@ -631,19 +625,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (need_any) {
                 // exact tile maximum per row -> new reference max; rescale row sums and O
 #pragma unroll
-                for (int i = 0; i < RH; ++i) {
+                for (int i = 0; i < kGroupRows; ++i) {
                     const float m = warp_max(((validm >> i) & 1u) ? y[i] : -INFINITY);
-                    if (lane == 0) sm.red[wg][wq][i] = m;
+                    if (lane == 0) sm.red[g][wq][i] = m;
                 }
-                ok = wg_sync(ctx, wg, wq, epoch, false, nullptr);
+                ok = wg_sync(ctx, g, wq, epoch, false, nullptr);
                 float mnew_own = 0.f;
                 bool own = false;
                 if (ok) {
 #pragma unroll
-                    for (int i = 0; i < RH; ++i) {
-                        const float mo = -sm.negm[row0 + i];
-                        const float tm = fmaxf(fmaxf(sm.red[wg][0][i], sm.red[wg][1][i]),
-                                               fmaxf(sm.red[wg][2][i], sm.red[wg][3][i]));
+                    for (int i = 0; i < kGroupRows; ++i) {
+                        const float mo = kPShift - sm.negm[row0 + i];
+                        const float tm = fmaxf(fmaxf(sm.red[g][0][i], sm.red[g][1][i]),
+                                               fmaxf(sm.red[g][2][i], sm.red[g][3][i]));
                         const float mn = fmaxf(mo, tm);
                         const float alpha = (mn == -INFINITY) ? 1.f : ex2(mo - mn);
                         lsum[i] *= alpha;
@@ -653,93 +647,102 @@ __global__ void __launch_bounds__(kThreads, 1)
                             own = true;
                         }
                     }
-                    ok = wg_sync(ctx, wg, wq, epoch, false, nullptr);  // alphas visible, old m read
-                    if (own) sm.negm[row0 + st] = -mnew_own;
-                    ok = ok && wg_sync(ctx, wg, wq, epoch, false, nullptr);  // new m visible
+                    ok = wg_sync(ctx, g, wq, epoch, false, nullptr);  // alphas visible, old m read
+                    if (own) sm.negm[row0 + st] = kPShift - mnew_own;
+                    ok = ok && wg_sync(ctx, g, wq, epoch, false, nullptr);  // new m visible
                 }
                 if (ok && t > 0) {
                     // O holds tiles < t: wait for their PV, then scale this group's row columns
-                    ok = ctx.wait_warp(&sm.pempty[(t - 1) % kPStages], ((t - 1) / kPStages) & 1);
+                    // of all three terms in both head-dim halves
+                    ok = ctx.wait_warp(&sm.pempty[(t - 1) % kPStages],
+                                       ((t - 1) / kPStages) & 1);
                     if (ok) {
                         tc_fence_after();
+#pragma unroll 1
+                        for (int sl = 0; sl < 2 * kTerms; ++sl) {
+                            const int dh = sl / kTerms, term = sl % kTerms;
+                            const uint32_t addr =
+                                lane_base + C::kColO + dh * SN + term * RP + row0;
+                            uint32_t o[16];
+                            tmem_ld16(addr, o);
+                            tmem_ld_wait(o);
 #pragma unroll
-                        for (int dh = 0; dh < 2; ++dh) {
-                            uint32_t o[RH];
-                            const uint32_t oaddr = lane_base + kColO + dh * kOStride + row0;
-                            tmem_load_cols<RH>(oaddr, o);
-                            tmem_ld_wait_n<RH>(o);
-#pragma unroll
-                            for (int i = 0; i < RH; ++i)
+                            for (int i = 0; i < 16; ++i)
                                 o[i] = __float_as_uint(f32(o[i]) * sm.alpha[row0 + i]);
-                            tmem_store_cols<RH>(oaddr, o);
+                            tmem_st16(addr, o);
                         }
                         tmem_st_wait();
                     }
                 }
             }
-            // pass 2: probabilities -> FP16 P (MN-major: this thread's rows, contiguous), row sums
+            // pass 2: probabilities -> three E4M3 terms in P (this thread's 16 rows of each term
+            // are one 16-byte chunk), row sums from the unrounded values
             const int ps = t % kPStages;
             if (ok) ok = ctx.wait_warp(&sm.pempty[ps], ((t / kPStages) & 1) ^ 1);
             if (!ok) {
                 alive = false;
                 break;
             }
-            uint8_t* pbuf = smem + kOffP + ps * kPStage;
+            uint32_t code[kTerms][4];
 #pragma unroll
-            for (int c = 0; c < RH / 8; ++c) {
-                uint32_t w[4];
+            for (int w = 0; w < 4; ++w) {
+                const float4 nm = negmv[w];
+                float pv[4];
+                pv[0] = ((validm >> (4 * w + 0)) & 1u) ? ex2(y[4 * w + 0] + nm.x) : 0.f;
+                pv[1] = ((validm >> (4 * w + 1)) & 1u) ? ex2(y[4 * w + 1] + nm.y) : 0.f;
+                pv[2] = ((validm >> (4 * w + 2)) & 1u) ? ex2(y[4 * w + 2] + nm.z) : 0.f;
+                pv[3] = ((validm >> (4 * w + 3)) & 1u) ? ex2(y[4 * w + 3] + nm.w) : 0.f;
 #pragma unroll
-                for (int q2 = 0; q2 < 4; ++q2) {
-                    const int i0 = c * 8 + 2 * q2, i1 = i0 + 1;
-                    const float p0 = ((validm >> i0) & 1u) ? ex2(y[i0] + sm.negm[row0 + i0]) : 0.f;
-                    const float p1 = ((validm >> i1) & 1u) ? ex2(y[i1] + sm.negm[row0 + i1]) : 0.f;
-                    lsum[i0] += p0;
-                    lsum[i1] += p1;
-                    const __half2 hp = __floats2half2_rn(p0, p1);
-                    w[q2] = *reinterpret_cast<const uint32_t*>(&hp);
-                }
-                *reinterpret_cast<uint4*>(pbuf + mnmajor_chunk(row0 + c * 8, st, kPStage)) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
+                for (int e = 0; e < 4; ++e) lsum[4 * w + e] += pv[e];
+                uint32_t h01, m01, l01, h23, m23, l23;
+                split3_x2(pv[0], pv[1], h01, m01, l01);
+                split3_x2(pv[2], pv[3], h23, m23, l23);
+                code[0][w] = h01 | (h23 << 16);
+                code[1][w] = m01 | (m23 << 16);
+                code[2][w] = l01 | (l23 << 16);
             }
+            uint8_t* pbuf = smem + C::kOffP + ps * C::kPStage;
+#pragma unroll
+            for (int term = 0; term < kTerms; ++term)
+                *reinterpret_cast<uint4*>(pbuf + p_chunk(term * C::kGroups + g, st)) =
+                    make_uint4(code[term][0], code[term][1], code[term][2], code[term][3]);
             fence_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sm.pfull[ps]));
         }
-        // row sums over the 128 key lanes -> split state
+        // row sums over the 128 key lanes -> split state (max m - s, shifted sums and numerator)
 #pragma unroll
-        for (int i = 0; i < RH; ++i) {
+        for (int i = 0; i < kGroupRows; ++i) {
             const float v = warp_sum(lsum[i]);
-            if (lane == 0) sm.red[wg][wq][i] = v;
+            if (lane == 0) sm.red[g][wq][i] = v;
         }
-        if (alive) alive = wg_sync(ctx, wg, wq, epoch, false, nullptr);
+        if (alive) alive = wg_sync(ctx, g, wq, epoch, false, nullptr);
         const int64_t unit = ((int64_t)b * p.num_kv_heads + h) * p.num_splits + split;
         if (alive && !ctx.aborted()) {
 #pragma unroll
-            for (int i = 0; i < RH; ++i) {
+            for (int i = 0; i < kGroupRows; ++i) {
                 if (st == i && row0 + i < R) {
-                    const float L = sm.red[wg][0][i] + sm.red[wg][1][i] + sm.red[wg][2][i] +
-                                    sm.red[wg][3][i];
+                    const float L = sm.red[g][0][i] + sm.red[g][1][i] + sm.red[g][2][i] +
+                                    sm.red[g][3][i];
                     p.ws_state[unit * R + row0 + i] = make_float2(-sm.negm[row0 + i], L);
                 }
             }
         }
-        // O^T (tensor memory, lane = head-dim element) -> numerator rows; group wg writes half wg
+        // O^T (tensor memory, lane = head-dim element) -> numerator rows: O = O_h + O_m/16 + O_l/256
         const bool ok = ctx.wait_warp(&sm.odone, 0);
         tc_fence_after();
         if (__all_sync(0xffffffffu, ok && !ctx.aborted())) {
             const float vs = __ldg(p.v_scale);
-            const int d = wg * 128 + st;
-            const uint32_t base = lane_base + kColO + wg * kOStride;
+#pragma unroll 1
+            for (int dh = 0; dh < 2; ++dh) {
+                float o[kGroupRows];
+                load_terms16<RP>(lane_base + C::kColO + dh * SN + row0, o);
+                const int d = dh * 128 + st;
 #pragma unroll
-            for (int rc = 0; rc < RP / 8; ++rc) {
-                uint32_t o[8];
-                tmem_ld8(base + rc * 8, o);
-                tmem_ld_wait_n<8>(o);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int r = rc * 8 + e;
-                    if (r < R) p.ws_acc[(unit * R + r) * kHeadDim + d] = f32(o[e]) * vs;
+                for (int i = 0; i < kGroupRows; ++i) {
+                    const int r = row0 + i;
+                    if (r < R) p.ws_acc[(unit * R + r) * kHeadDim + d] = o[i] * vs;
                 }
             }
         }
@@ -749,17 +752,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, C::kTmemCols);
     }
 }
 
 }  // namespace tc
 
-int tc_rows_pad(int rows) { return (rows + 15) / 16 * 16; }
+int tc_rows_pad(int rows) { return (rows + tc::kGroupRows - 1) / tc::kGroupRows * tc::kGroupRows; }
 
 bool tc_supports(int rows) { return tc_rows_pad(rows) <= tc::kMaxRP; }
 
-size_t tc_smem_bytes() { return tc::kSmemBytes; }
+size_t tc_smem_bytes(int rows) {
+    switch (tc_rows_pad(rows)) {
+        case 16: return tc::smem_bytes<16>();
+        case 32: return tc::smem_bytes<32>();
+        default: return tc::smem_bytes<48>();
+    }
+}
+
+int tc_threads(int rows) {
+    switch (tc_rows_pad(rows)) {
+        case 16: return tc::Cfg<16>::kThreads;
+        case 32: return tc::Cfg<32>::kThreads;
+        default: return tc::Cfg<48>::kThreads;
+    }
+}
 
 // The tensor-map encoder lives in the driver library; it is looked up at first use through the
 // runtime (so the library itself loads on machines without a driver, e.g. to plan and test).
@@ -782,12 +799,12 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 template <int RP>
 static cudaError_t launch_rp(const CUtensorMap& kmap, const CUtensorMap& vmap,
                              const PartialParams& p, cudaStream_t stream) {
+    constexpr uint32_t smem = tc::smem_bytes<RP>();
     cudaError_t e = cudaFuncSetAttribute(tc::tc_partial_kernel<RP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         tc::kSmemBytes);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(p.num_splits, p.num_kv_heads, p.batch);
-    tc::tc_partial_kernel<RP><<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(kmap, vmap, p);
+    tc::tc_partial_kernel<RP><<<grid, tc::Cfg<RP>::kThreads, smem, stream>>>(kmap, vmap, p);
     return cudaGetLastError();
 }
 
@@ -796,20 +813,21 @@ cudaError_t launch_tc_partial(const PartialParams& p, cudaStream_t stream) {
     if (rp > tc::kMaxRP) return cudaErrorInvalidValue;
     const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
+    // K and V pools viewed as [num_pages * page_size rows, Hkv * 256 bytes]; both copied in boxes
+    // of 16 rows x 128 bytes into the 128-byte swizzle the MMA operands use
     CUtensorMap kmap, vmap;
     const cuuint64_t dims[2] = {(cuuint64_t)p.num_kv_heads * kHeadDim,
                                 (cuuint64_t)p.num_pages * p.page_size};
     const cuuint64_t strides[1] = {(cuuint64_t)p.num_kv_heads * kHeadDim};
-    const cuuint32_t kbox[2] = {128, tc::kChunk};
-    const cuuint32_t vbox[2] = {kHeadDim, tc::kChunk};
+    const cuuint32_t box[2] = {128, tc::kChunk};
     const cuuint32_t estride[2] = {1, 1};
     CUresult r1 = encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.k_pool),
-                         dims, strides, kbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     CUresult r2 = encode(&vmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.v_pool),
-                         dims, strides, vbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r1 != CUDA_SUCCESS || r2 != CUDA_SUCCESS) return cudaErrorInvalidValue;
     switch (rp) {
