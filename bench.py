@@ -44,6 +44,8 @@ def parse_args():
     ap.add_argument("--splits", type=int, default=0, help="force the split count (0: planner)")
     ap.add_argument("--layers", type=int, default=0,
                     help="time only the first L layers (profiling captures; 0: all)")
+    ap.add_argument("--fused-combine", action="store_true",
+                    help="merge the splits inside the partial launch (one kernel per layer)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -225,7 +227,8 @@ def run_ours(args, rank, world, local_rank):
     build_mod.build()
     w = workload(args.config)
     stack = LayerStack(w, device=dev, num_splits=args.splits, kernel=args.kernel,
-                       layers=args.layers or None)
+                       layers=args.layers or None,
+                       flags=B.DFLASH_PROBLEM_FUSED_COMBINE if args.fused_combine else 0)
     plan = stack.plan
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = None
@@ -258,9 +261,11 @@ def run_ours(args, rank, world, local_rank):
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     ms = max_over_ranks(statistics.mean(step_ms), world, dev)
 
-    # kernel attribution: the same 16 partial launches (and, separately, the 16 combine launches)
-    # replayed from their own graphs, CUDA events around each replay on the replay stream
-    g_partial, g_combine = stack.capture_kernel_graphs()
+    # kernel attribution: with the merge fused into the partial kernel, a step is one launch per
+    # layer and the kernel time is the step time per layer; otherwise the same 16 partial
+    # launches (and, separately, the 16 combine launches) are replayed from their own graphs,
+    # CUDA events around each replay on the replay stream
+    fused = bool(plan.combine_fused)
     nl = len(stack.layers)
 
     def timed_replays(graph):
@@ -278,8 +283,13 @@ def run_ours(args, rank, world, local_rank):
         barrier()
         return statistics.mean(a.elapsed_time(b) for a, b in ev) / nl
 
-    partial_ms = timed_replays(g_partial)
-    combine_ms = timed_replays(g_combine)
+    if fused:
+        partial_ms = statistics.mean(step_ms) / nl
+        combine_ms = 0.0
+    else:
+        g_partial, g_combine = stack.capture_kernel_graphs()
+        partial_ms = timed_replays(g_partial)
+        combine_ms = timed_replays(g_combine)
 
     # end to end through the public API: per step, H2D of the step's inputs from pinned host
     # memory (Q, block tables, context lengths, scales of all layers), the 16 layers, and D2H of
@@ -322,9 +332,11 @@ def run_ours(args, rank, world, local_rank):
 
     nbytes = algorithmic_bytes(w, plan)
     peak, peak_kind = measured_peak()
-    achieved = nbytes["partial"] / (partial_ms * 1e-3) / 1e9
+    launch_bytes = nbytes["partial"] + (nbytes["combine"] if fused else 0)
+    achieved = launch_bytes / (partial_ms * 1e-3) / 1e9
     src_hash = kernel_source_hash()
-    ktag = {1: "simt_partial", 2: "tc_partial"}.get(plan.kernel, "partial")
+    ktag = {1: "simt_partial", 2: "tc_fused" if fused else "tc_partial"}.get(plan.kernel,
+                                                                           "partial")
     traffic = ncu_traffic(ktag, w.name, src_hash)
     step_bytes = (nbytes["partial"] + nbytes["combine"]) * nl
     cpu = None
@@ -348,7 +360,7 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32" if plan.kernel == B.DFLASH_KERNEL_SIMT else "f16*f16->f32",
+        "dtype": "f32" if plan.kernel == B.DFLASH_KERNEL_SIMT else "e4m3->f32",
         "data": "synthetic",
         "config": {
             "workload": w.name, "layers": w.layers, "batch": w.batch, "q_len": w.q_len,
@@ -365,16 +377,18 @@ def run_ours(args, rank, world, local_rank):
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": traffic,
             "peak_kind": peak_kind, "kernel": ktag,
-            "kernel_ms": round(partial_ms, 5), "bytes_per_launch": nbytes["partial"],
+            "kernel_ms": round(partial_ms, 5), "bytes_per_launch": launch_bytes,
         },
         "step_hbm_gbs": round(step_bytes / (ms * 1e-3) / 1e9, 1),
         "step_frac_of_peak": round(step_bytes / (ms * 1e-3) / 1e9 / peak, 4),
         "combine_kernel_ms": round(combine_ms, 5),
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 2 * nl * args.steps,
-        "kernel_timing": "per-kernel times from graph replays of the 16 partial (or combine) "
-                         "launches alone, CUDA events on the replay stream",
+        "gpu_launches": (1 if fused else 2) * nl * args.steps,
+        "kernel_timing": ("one fused launch per layer: kernel time = timed step / layers"
+                          if fused else
+                          "per-kernel times from graph replays of the 16 partial (or combine) "
+                          "launches alone, CUDA events on the replay stream"),
         "clocks": clocks.summary(),
         "kernel_source_hash": src_hash,
     }

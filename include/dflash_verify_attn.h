@@ -49,8 +49,11 @@
  *     DFLASH_ERR_WORKSPACE_TOO_SMALL without launching anything.
  *   - Device-only conditions never fault. A context above plan.problem.max_context is clamped to
  *     it, a block-table entry outside [0, num_pages) is clamped into range, and each sets a bit in
- *     the sticky status word at the head of the workspace (DFLASH_FLAG_*). The caller zeroes that
- *     word once when allocating the workspace (dflash_verify_attn_read_flags can clear it).
+ *     the sticky status word at the head of the workspace (DFLASH_FLAG_*). The caller zeroes the
+ *     first 16 bytes of the workspace once when allocating it: the status word (offset 0,
+ *     dflash_verify_attn_read_flags can clear it) and the 64-bit grid-barrier counter of the
+ *     fused merge (offset 8; it needs no reset between calls, but zero it again after a
+ *     DFLASH_FLAG_KERNEL_TIMEOUT).
  *   - Launch failures map to DFLASH_ERR_CUDA (cudaGetLastError, which does not synchronise).
  */
 #ifndef DFLASH_VERIFY_ATTN_H
@@ -79,6 +82,9 @@ typedef enum {
 #define DFLASH_FLAG_PAGE_CLAMPED 0x4     /* a block-table entry outside [0, num_pages): clamped */
 #define DFLASH_FLAG_KERNEL_TIMEOUT 0x8   /* a tensor-core kernel wait gave up; outputs invalid */
 
+/* Bits of dflash_verify_attn_problem.flags. */
+#define DFLASH_PROBLEM_FUSED_COMBINE 0x1 /* forward merges the splits inside the partial launch */
+
 /* Partial-attention kernel variants a plan can select. */
 #define DFLASH_KERNEL_AUTO 0
 #define DFLASH_KERNEL_SIMT 1     /* CUDA-core FP32 kernel: any supported shape */
@@ -99,7 +105,7 @@ typedef struct {
     int32_t device;            /* CUDA ordinal whose SM count sizes the plan */
     int32_t num_splits;        /* 0: planner's choice; > 0 forces the split count */
     int32_t kernel;            /* DFLASH_KERNEL_*; AUTO picks the fastest supported */
-    int32_t reserved;
+    int32_t flags;             /* DFLASH_PROBLEM_* bits; 0 for the defaults */
 } dflash_verify_attn_problem;
 
 /* Written by dflash_verify_attn_plan, read-only afterwards. Host POD; copy freely. */
@@ -113,7 +119,7 @@ typedef struct {
     int32_t threads;          /* partial-kernel block size */
     int32_t smem_bytes;       /* partial-kernel dynamic shared memory */
     int32_t sm_count;         /* SMs of plan.problem.device */
-    int32_t reserved;
+    int32_t combine_fused;    /* 1: forward merges the splits inside the partial-kernel launch */
     size_t workspace_bytes;   /* caller allocates at least this many bytes */
     size_t ws_state_offset;   /* float2 (m, l) [batch, Hkv, S, R]; m in log2 units */
     size_t ws_acc_offset;     /* float numerator [batch, Hkv, S, R, head_dim], v_scale applied */
@@ -162,7 +168,13 @@ int dflash_verify_attn_combine(const dflash_verify_attn_plan_t* plan, const void
                                size_t workspace_bytes, const int32_t* context_lens, void* out,
                                float* lse, void* cuda_stream);
 
-/* run followed by combine on one stream. */
+/*
+ * run followed by combine on one stream. With DFLASH_PROBLEM_FUSED_COMBINE in problem.flags (tensor-core kernel, batch * num_kv_heads <=
+ * the SM count; plan->combine_fused tells), both happen in a single cooperative launch of the
+ * partial kernel instead: after every CTA has written its split state (a bounded grid-wide
+ * barrier on the workspace header), the CTAs share out the combine's work and write out and lse
+ * themselves. Results are the same as run + combine (same merge arithmetic).
+ */
 int dflash_verify_attn_forward(const dflash_verify_attn_plan_t* plan, const void* q,
                                const void* k_pool, const void* v_pool,
                                const int32_t* block_table, const int32_t* context_lens,

@@ -24,6 +24,7 @@ DFLASH_ERR_CUDA = -4
 DFLASH_FLAG_CONTEXT_CLAMPED = 0x1
 DFLASH_FLAG_CONTEXT_SHORT = 0x2
 DFLASH_FLAG_PAGE_CLAMPED = 0x4
+DFLASH_PROBLEM_FUSED_COMBINE = 0x1
 DFLASH_KERNEL_AUTO = 0
 DFLASH_KERNEL_SIMT = 1
 DFLASH_KERNEL_TCGEN05 = 2
@@ -45,13 +46,13 @@ class Problem(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "version", "batch", "q_len", "num_q_heads", "num_kv_heads", "head_dim", "page_size",
         "max_pages_per_seq", "num_pages", "max_context", "device", "num_splits", "kernel",
-        "reserved")]
+        "flags")]
 
 
 class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "version", "kernel", "num_splits", "tile_keys", "min_split_keys", "rows", "threads",
-        "smem_bytes", "sm_count", "reserved")] + [
+        "smem_bytes", "sm_count", "combine_fused")] + [
         ("workspace_bytes", ctypes.c_size_t),
         ("ws_state_offset", ctypes.c_size_t),
         ("ws_acc_offset", ctypes.c_size_t),
@@ -133,10 +134,10 @@ def _stream(stream):
 
 def make_problem(batch, q_len, num_q_heads, num_kv_heads, head_dim, page_size,
                  max_pages_per_seq, num_pages, max_context, device=0, num_splits=0,
-                 kernel=DFLASH_KERNEL_AUTO) -> Problem:
+                 kernel=DFLASH_KERNEL_AUTO, flags=0) -> Problem:
     return Problem(DFLASH_VERIFY_ATTN_VERSION, batch, q_len, num_q_heads, num_kv_heads,
                    head_dim, page_size, max_pages_per_seq, num_pages, max_context, device,
-                   num_splits, kernel, 0)
+                   num_splits, kernel, flags)
 
 
 def dflash_verify_attn_plan(problem: Problem) -> Plan:
@@ -231,12 +232,12 @@ class VerifyAttention:
 
     def __init__(self, batch, q_len, num_q_heads, num_kv_heads, head_dim, page_size,
                  max_pages_per_seq, num_pages, max_context, device=None, num_splits=0,
-                 kernel=DFLASH_KERNEL_AUTO, workspace=None):
+                 kernel=DFLASH_KERNEL_AUTO, workspace=None, flags=0):
         dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
         self.device = dev
         self.problem = make_problem(batch, q_len, num_q_heads, num_kv_heads, head_dim,
                                     page_size, max_pages_per_seq, num_pages, max_context,
-                                    dev.index, num_splits, kernel)
+                                    dev.index, num_splits, kernel, flags)
         self.plan = dflash_verify_attn_plan(self.problem)
         if workspace is None:
             workspace = torch.zeros(self.plan.workspace_bytes, dtype=torch.uint8, device=dev)

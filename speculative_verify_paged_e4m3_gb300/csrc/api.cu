@@ -30,6 +30,7 @@ namespace {
 
 constexpr int kDefaultSmCount = 152;  // GB300
 constexpr size_t kHeaderBytes = 256;
+constexpr size_t kGridBarrierOffset = 8;  // 64-bit ticket counter of the fused merge's barrier
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -80,6 +81,9 @@ PartialParams partial_params(const dflash_verify_attn_plan_t* plan, const void* 
     p.num_splits = plan->num_splits;
     p.tile_keys = plan->tile_keys;
     p.min_split_keys = plan->min_split_keys;
+    p.grid_bar = reinterpret_cast<unsigned long long*>(ws + kGridBarrierOffset);
+    p.out = nullptr;  // partial state only; forward() sets these for a fused launch
+    p.lse = nullptr;
     return p;
 }
 
@@ -145,8 +149,18 @@ int dflash_verify_attn_plan(const dflash_verify_attn_problem* pr,
         plan->smem_bytes = (int32_t)simt_smem_bytes();
     }
     const int64_t units = (int64_t)pr->batch * pr->num_kv_heads;
+    // On request the tensor-core kernel merges the splits itself (one launch per forward), which
+    // needs its whole grid on the GPU at once (one CTA per SM): the split count is then kept to
+    // floor(SMs / units).
+    const bool fuse = use_tc && (pr->flags & DFLASH_PROBLEM_FUSED_COMBINE) &&
+                      units <= sm_count &&
+                      (pr->num_splits == 0 || units * pr->num_splits <= sm_count);
     int64_t S = pr->num_splits;
-    if (S == 0) {
+    if (S == 0 && fuse) {
+        S = sm_count / units;
+        const int64_t cap = ceil_div(pr->max_context, plan->min_split_keys);
+        if (S > cap) S = cap;
+    } else if (S == 0) {
         S = ceil_div(sm_count, units);  // one wave of single-CTA-per-SM work
         const int64_t cap = ceil_div(pr->max_context, plan->min_split_keys);
         if (S > cap) S = cap;
@@ -154,6 +168,7 @@ int dflash_verify_attn_plan(const dflash_verify_attn_problem* pr,
     if (S < 1) S = 1;
     if (S > 65535) return DFLASH_ERR_UNSUPPORTED;
     plan->num_splits = (int32_t)S;
+    plan->combine_fused = fuse ? 1 : 0;
     plan->rows = (int32_t)rows;
     plan->sm_count = sm_count;
     const size_t state_bytes = (size_t)units * S * rows * sizeof(float2);
@@ -251,6 +266,28 @@ int dflash_verify_attn_forward(const dflash_verify_attn_plan_t* plan, const void
                                const int32_t* block_table, const int32_t* context_lens,
                                const float* k_scale, const float* v_scale, void* workspace,
                                size_t workspace_bytes, void* out, float* lse, void* cuda_stream) {
+    if (plan && plan->combine_fused) {
+        int rc = check_plan(plan);
+        if (rc != DFLASH_OK) return rc;
+        if (plan->kernel != DFLASH_KERNEL_TCGEN05) return DFLASH_ERR_INVALID_ARGUMENT;
+        if (!q || !k_pool || !v_pool || !block_table || !context_lens || !k_scale || !v_scale ||
+            !workspace || !out || !lse)
+            return DFLASH_ERR_INVALID_ARGUMENT;
+        if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+            !aligned(workspace, 256) || !aligned(block_table, 4) || !aligned(context_lens, 4) ||
+            !aligned(out, 8) || !aligned(lse, 4))
+            return DFLASH_ERR_INVALID_ARGUMENT;
+        if (workspace_bytes < plan->workspace_bytes) return DFLASH_ERR_WORKSPACE_TOO_SMALL;
+        PartialParams p = partial_params(plan, q, k_pool, v_pool, block_table, context_lens,
+                                         k_scale, v_scale, workspace);
+        p.out = static_cast<__half*>(out);
+        p.lse = lse;
+        if (launch_tc_partial(p, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) {
+            cudaGetLastError();
+            return DFLASH_ERR_CUDA;
+        }
+        return DFLASH_OK;
+    }
     int rc = dflash_verify_attn_run(plan, q, k_pool, v_pool, block_table, context_lens, k_scale,
                                     v_scale, workspace, workspace_bytes, cuda_stream);
     if (rc != DFLASH_OK) return rc;

@@ -1,0 +1,123 @@
+// combine_impl.cuh -- the merge of per-split FP32 state into FP16 output and FP32 log-sum-exp,
+// shared by the standalone combine kernel and the partial kernel's fused merge.
+//
+// The pages pair every grouped q8 attention kernel with one combine kernel ("[Perf] Reduce
+// DFlash2 attention cost and screen exact QK reuse", Test Result). For query row r the active
+// splits s carry (m_s, l_s, acc_s) with m in log2 units:
+//   M = max_s m_s, L = sum_s 2^{m_s - M} l_s, out = sum_s 2^{m_s - M} acc_s / L,
+//   lse = (M + log2 L) * ln 2.
+// One work item is (query row, quarter of the head dim, sequence x KV head), done by 256 threads:
+// 16 split lanes x 16 float4 columns, so the splits are read in parallel (16 at a time, each a
+// coalesced 256-byte row segment) and reduced through shared memory. The merge is associative,
+// so a lane may fold its splits in any grouping: out and lse are the same sums in another order.
+#pragma once
+
+#include <math.h>
+
+#include "common.cuh"
+
+namespace dflash {
+
+constexpr int kCombineThreads = 256;
+constexpr int kCombineSplitLanes = 16;  // splits in flight per item
+constexpr int kCombineCols = 16;        // float4 columns per item (64 head-dim elements)
+constexpr int kCombineFold = 10;        // splits per lane whose loads are in flight together
+
+struct CombineScratch {
+    float4 part[kCombineSplitLanes][kCombineCols];
+    float2 ml[kCombineSplitLanes];  // (running max, running sum) of each split lane
+};
+
+__device__ __forceinline__ void combine_sync(int bar_id) {
+    asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(kCombineThreads) : "memory");
+}
+
+// Merge item (row r, head-dim quarter, sequence b, KV head h). tid in [0, 256) indexes the 256
+// threads that share named barrier bar_id and scratch sh. Each split lane folds its splits
+// (sl, sl + 16, ...) into a running (max, sum, numerator) in one pass, so that all its loads can
+// be in flight at once; the 16 lanes are then merged the same way through shared memory. The split
+// state is read through L2 (ld.global.cg), so that state written by other CTAs of the same launch
+// is seen.
+// n_raw: context_lens[b] when the caller has loaded it already, else -1.
+__device__ __forceinline__ void combine_item(const CombineParams& p, int r, int quarter, int b,
+                                             int h, int tid, int bar_id, CombineScratch& sh,
+                                             int n_raw = -1) {
+    const int sl = tid / kCombineCols, col = tid % kCombineCols;
+    int n = n_raw >= 0 ? n_raw : p.context_lens[b];
+    n = n > p.max_context ? p.max_context : n;
+    const int per = keys_per_split(n, p.num_splits, p.tile_keys, p.min_split_keys);
+    const int active = n > 0 ? (n + per - 1) / per : 0;
+    const int64_t base = ((int64_t)b * p.num_kv_heads + h) * p.num_splits;
+    const int R = p.rows;
+    const float4* acc4 = reinterpret_cast<const float4*>(p.ws_acc);
+
+    float m = -INFINITY, L = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = sl; s0 < active; s0 += kCombineSplitLanes * kCombineFold) {
+        // all loads of kCombineFold splits first (one round trip), then the fold; an active split
+        // always has its numerator written (zero for a row it does not see)
+        float2 st[kCombineFold];
+        float4 a[kCombineFold];
+#pragma unroll
+        for (int k = 0; k < kCombineFold; ++k) {
+            // unconditional loads (index clamped into the allocation), masked afterwards
+            const int s = min(s0 + k * kCombineSplitLanes, active - 1);
+            st[k] = __ldcg(&p.ws_state[(base + s) * R + r]);
+            a[k] = __ldcg(&acc4[((base + s) * R + r) * (kHeadDim / 4) + quarter * kCombineCols + col]);
+        }
+#pragma unroll
+        for (int k = 0; k < kCombineFold; ++k) {
+            if (s0 + k * kCombineSplitLanes >= active) {
+                st[k] = make_float2(-INFINITY, 0.f);
+                a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            const float mn = fmaxf(m, st[k].x);
+            const float cr = mn == -INFINITY ? 1.f : exp2f(m - mn);
+            const float cs = mn == -INFINITY ? 0.f : exp2f(st[k].x - mn);
+            L = fmaf(cs, st[k].y, L * cr);
+            o.x = fmaf(cs, a[k].x, o.x * cr);
+            o.y = fmaf(cs, a[k].y, o.y * cr);
+            o.z = fmaf(cs, a[k].z, o.z * cr);
+            o.w = fmaf(cs, a[k].w, o.w * cr);
+            m = mn;
+        }
+    }
+    sh.part[sl][col] = o;
+    if (col == 0) sh.ml[sl] = make_float2(m, L);
+    combine_sync(bar_id);
+    if (tid < kCombineCols) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kCombineSplitLanes; ++k) M = fmaxf(M, sh.ml[k].x);
+        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+        float Lt = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int k = 0; k < kCombineSplitLanes; ++k) {
+                const float2 ml = sh.ml[k];
+                const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+                const float4 q = sh.part[k][tid];
+                t.x = fmaf(w, q.x, t.x);
+                t.y = fmaf(w, q.y, t.y);
+                t.z = fmaf(w, q.z, t.z);
+                t.w = fmaf(w, q.w, t.w);
+                Lt = fmaf(w, ml.y, Lt);
+            }
+            t.x /= Lt;
+            t.y /= Lt;
+            t.z /= Lt;
+            t.w /= Lt;
+        }
+        const int i = r / p.group, g = r % p.group;
+        const int64_t orow = ((int64_t)b * p.q_len + i) * p.num_q_heads + h * p.group + g;
+        __half2* out2 =
+            reinterpret_cast<__half2*>(p.out + orow * kHeadDim + (quarter * kCombineCols + tid) * 4);
+        out2[0] = __floats2half2_rn(t.x, t.y);
+        out2[1] = __floats2half2_rn(t.z, t.w);
+        if (quarter == 0 && tid == 0)
+            p.lse[orow] = (M == -INFINITY) ? -INFINITY : (M + log2f(Lt)) * kLn2;
+    }
+    combine_sync(bar_id);  // the scratch is reused by the next item
+}
+
+}  // namespace dflash

@@ -27,6 +27,11 @@ struct PartialParams {
     int batch, q_len, num_q_heads, num_kv_heads, group, rows;
     int page_size, max_pages_per_seq, num_pages, max_context;
     int num_splits, tile_keys, min_split_keys;
+    // merge of the splits inside the same launch (every CTA resident): grid barrier words in the
+    // workspace header, then FP16 output and FP32 log-sum-exp; null out when not fused
+    unsigned long long* grid_bar;  // ticket counter of the grid barrier (workspace header)
+    __half* out;
+    float* lse;
 };
 
 struct CombineParams {

@@ -16,8 +16,9 @@
 //    k_scale / 16 * log2 e.
 //  * The probabilities, taken as p = 2^(s - m) * 2^score with s = 4 and a reference max m (so
 //    p <= 2^8, see below), are split the same way into three E4M3 terms p = h + m/16 + l/256
-//    (Veltkamp splitting in FP32, relative error about 2^-12, finer than an FP16 P), stacked on N,
-//    so O^T accumulates three FP32 terms that are summed at the end. The shift s keeps the leading
+//    (h and m truncated to 4 significant bits, residuals exact, l rounded: relative error about
+//    2^-12, finer than an FP16 P), stacked on N, so O^T accumulates three FP32 terms that are
+//    summed at the end. The shift s keeps the leading
 //    term out of E4M3's subnormal range down to p = 2^-10 of the reference: below 2^-6 the
 //    leading term only has a 2^-9 grid, and over 10^5 keys those roundings add up.
 //  * Softmax: keys on tensor-memory lanes (thread = key); RP/16 warpgroups of 16 query rows each.
@@ -25,12 +26,22 @@
 //    2^(8 - s) (then the warpgroup rescales its O columns in tensor memory), and FP32 row sums of
 //    the unrounded (shifted) probabilities, reduced across the key lanes once per split. The
 //    split state keeps m - s as its max, which makes the shift invisible to the combine.
-//  * Warp roles: warp 0 copies K tiles (TMA, 2 stages of 128 keys); warp 1 owns tensor memory and
-//    issues the MMAs; warp 2 copies V (TMA, 64-key stages) and zeroes the keys past the context
-//    in the last one (a zero probability must not meet a NaN code); warps 4.. stage the Q terms
-//    (while the first copies are in flight), then run the softmax and write O out. K and V copies
-//    come from two different warps: one issuing warp tops out well below the HBM rate on this GPU
-//    (measured), two reach it.
+//  * Warp roles: warps 0 and 3 copy K tiles (TMA, 2 stages of 128 keys, half of each tile's
+//    chunks each); warp 2 copies V (TMA, 3 stages of 128 keys) and zeroes the keys past the
+//    context in the last one (a zero probability must not meet a NaN code); warp 1 owns tensor
+//    memory and issues the MMAs from one thread that polls both streams (QK of the next tile, PV
+//    of the next V stage) without blocking on either; warps 4.. stage the Q terms (while the first
+//    copies are in flight), then run the softmax and write O out. The copies come from three
+//    warps: on this GPU the copy throughput of one SM grows with the number of warps issuing them
+//    (measured with this very box pattern: 4.4, 6.2 and 6.6 TB/s over the whole GPU for one, two
+//    and three warps).
+//  * One P buffer, reused slice by slice: the softmax warp of lane quadrant q owns keys
+//    [32q, 32q + 32) of every tile, so it waits only for the PV step that read its slice of the
+//    previous tile; the MMAs of a V stage wait for the P slices they read.
+//  * The softmax math runs on FP32 pairs (f32x2 instructions), the warpgroup barriers on
+//    mbarriers (waiting warps are suspended instead of polling shared memory).
+//  * Optionally (fused combine) the CTAs of one launch meet at a grid barrier once every split
+//    state is written and merge the splits themselves.
 //    Every wait is bounded: on timeout the CTA sets DFLASH_FLAG_KERNEL_TIMEOUT, drains its copies
 //    and returns.
 #include <cuda.h>
@@ -41,6 +52,7 @@
 #include <cstddef>
 #include <mutex>
 
+#include "combine_impl.cuh"
 #include "common.cuh"
 #include "e4m3.cuh"
 #include "tc_ptx.cuh"
@@ -52,20 +64,21 @@ using namespace ptx;
 
 constexpr int kTile = 128;    // keys per tile = MMA M
 constexpr int kChunk = 16;    // keys per TMA box (pages are multiples of 16 tokens)
-constexpr int kVKeys = 64;    // keys per V stage
+constexpr int kVKeys = 128;   // keys per V stage (a whole tile: four 32-key MMA steps)
 constexpr int kTerms = 3;     // E4M3 terms of Q and of P
 constexpr int kMaxRP = 48;    // padded rows per KV head this kernel carries
 constexpr int kGroupRows = 16;
 constexpr int kKStages = 2;
-constexpr int kVStages = 5;
-constexpr int kPStages = 2;
+constexpr int kVStages = 3;
+constexpr int kSlices = kTile / 32;             // 32-key P slices of a tile (one per lane quadrant)
+constexpr int kSlicesPerStage = kVKeys / 32;    // slices a V stage's MMA step consumes
 
 constexpr uint32_t kKStage = kTile * kHeadDim;   // 32768: two 128-byte column blocks of 128 keys
-constexpr uint32_t kVStage = kVKeys * kHeadDim;  // 16384: two 128-byte column blocks of 64 keys
+constexpr uint32_t kVStage = kVKeys * kHeadDim;  // 32768: two 128-byte column blocks of 128 keys
 constexpr uint32_t kKHalf = kKStage / 2;
 constexpr uint32_t kVHalf = kVStage / 2;
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
-constexpr int kRowCache = 512;  // 16-key chunks of a split whose source row is looked up up front
+constexpr int kRowCache = 128;  // 16-key chunks of a split whose source row is looked up up front
 constexpr float kPShift = 4.f;         // s: probabilities are scaled by 2^s before the split
 constexpr float kLazyThreshold = 8.f;  // largest shifted probability exponent, 8 - s above the max
 
@@ -83,7 +96,7 @@ struct Cfg {
     static constexpr uint32_t kOffK = kOffQ + kQBytes;
     static constexpr uint32_t kOffV = kOffK + kKStages * kKStage;
     static constexpr uint32_t kOffP = kOffV + kVStages * kVStage;
-    static constexpr uint32_t kOffSmall = kOffP + kPStages * kPStage;
+    static constexpr uint32_t kOffSmall = kOffP + kPStage;  // one P buffer, reused per slice
     static constexpr uint32_t kColS = 0, kColO = SN;
     static constexpr uint32_t kTmemCols = 3 * SN <= 256 ? 256 : 512;
     static_assert(RP % kGroupRows == 0 && RP <= kMaxRP, "rows per CTA");
@@ -93,12 +106,14 @@ struct Cfg {
 };
 
 struct Small {
-    uint64_t kfull[kKStages], kempty[kKStages], sfull, sempty, pfull[kPStages], pempty[kPStages];
+    uint64_t kfull[kKStages], kempty[kKStages], sfull, sempty;
+    uint64_t pslice[kSlices];  // P slice q of the current tile written (one arrival per group)
     uint64_t vfull[kVStages], vfree[kVStages], vtail;
     uint64_t odone, qready;
+    uint64_t gbar[kMaxRP / kGroupRows];  // softmax group barriers (4 warp arrivals per phase)
     uint32_t tmem_base;
     int abort;
-    int flag[kMaxRP / kGroupRows][2][4];  // group barrier: [group][epoch parity][warp]
+    int gvote[kMaxRP / kGroupRows][2][4];  // group votes: [group][phase parity][warp]
     alignas(16) float c0[kMaxRP];    // score scale of each row (log2 units per MMA unit), float4 reads
     alignas(16) float negm[kMaxRP];  // s minus the reference max of each row (+inf: none yet), float4
     float red[kMaxRP / kGroupRows][4][kGroupRows];  // per-group, per-warp partials (max, row sums)
@@ -143,29 +158,25 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Split two probabilities (0 <= x <= 2^8) into three E4M3 terms x = h + m/16 + l/256 and return
-// the codes, two per 16-bit word (first value in the low byte). h and m are x and the scaled
-// residual rounded to 4 significant bits by Veltkamp splitting (c = x(2^20 + 1), h = c - (c - x),
-// exact in FP32 with round-to-nearest), so both are E4M3 values whenever they are at least 2^-6
-// and the residuals are exact; l is the last residual rounded to nearest by the conversion.
-__device__ __forceinline__ void split3_x2(float a, float b, uint32_t& h, uint32_t& m, uint32_t& l) {
-    constexpr float kC = 1048577.f;  // 2^20 + 1
-    const float ca = __fmul_rn(a, kC), cb = __fmul_rn(b, kC);
-    const float ha = __fsub_rn(ca, __fsub_rn(ca, a)), hb = __fsub_rn(cb, __fsub_rn(cb, b));
-    const float ra = __fmul_rn(__fsub_rn(a, ha), 16.f), rb = __fmul_rn(__fsub_rn(b, hb), 16.f);
-    const float da = __fmul_rn(ra, kC), db = __fmul_rn(rb, kC);
-    const float ma = __fsub_rn(da, __fsub_rn(da, ra)), mb = __fsub_rn(db, __fsub_rn(db, rb));
-    const float la = __fmul_rn(__fsub_rn(ra, ma), 16.f), lb = __fmul_rn(__fsub_rn(rb, mb), 16.f);
-    h = f32x2_to_e4m3x2(ha, hb);
-    m = f32x2_to_e4m3x2(ma, mb);
-    l = f32x2_to_e4m3x2(la, lb);
+// Bounded wait on an mbarrier phase (try_wait lets the hardware suspend the thread meanwhile):
+// gives up when the CTA's abort flag is raised or after kWaitLimitNs.
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, const volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 7) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        }
+    }
 }
 
 struct Ctx {
     Small* sm;
     int32_t* status;
     __device__ bool wait(uint64_t* bar, uint32_t parity) const {
-        if (mbar_wait(smem_u32(bar), parity, &sm->abort, kWaitLimitNs)) return true;
+        if (bar_wait(smem_u32(bar), parity, &sm->abort)) return true;
         *reinterpret_cast<volatile int*>(&sm->abort) = 1;
         atomicOr(status, DFLASH_FLAG_KERNEL_TIMEOUT);
         return false;
@@ -179,38 +190,32 @@ struct Ctx {
     __device__ bool aborted() const { return *reinterpret_cast<volatile int*>(&sm->abort) != 0; }
 };
 
-// Barrier of one softmax warpgroup (4 warps) through per-warp flags in shared memory, with a
-// bounded spin (a plain bar.sync could hang if one warp had given up). Each warp publishes
-// (epoch << 1) | vote; returns whether the barrier completed and ORs the four votes into *any.
-__device__ __forceinline__ bool wg_sync(const Ctx& ctx, int wg, int wq, int& epoch, bool vote,
-                                        bool* any) {
-    ++epoch;
+// Barrier of one softmax warpgroup (4 warps) on its mbarrier, in two halves so that work can go
+// on between them: group_arrive publishes this warp's vote (lane 0 stores it and arrives, with
+// release semantics) and returns the barrier phase; group_wait waits for that phase (acquire;
+// bounded, and suspended in hardware rather than spinning on shared memory) and ORs the four
+// votes into *any. A vote slot of phase e is rewritten only in phase e + 2, after every warp has
+// passed e + 1.
+__device__ __forceinline__ int group_arrive(const Ctx& ctx, int g, int wq, int& epoch, bool vote) {
+    const int e = epoch++;
     __syncwarp();
     if ((threadIdx.x & 31) == 0) {
-        __threadfence_block();
-        *reinterpret_cast<volatile int*>(&ctx.sm->flag[wg][epoch & 1][wq]) =
-            (epoch << 1) | (vote ? 1 : 0);
+        ctx.sm->gvote[g][e & 1][wq] = vote ? 1 : 0;
+        mbar_arrive(smem_u32(&ctx.sm->gbar[g]));
     }
-    // a warp can run at most one epoch ahead, so slot epoch & 1 holds this epoch or the one before
-    volatile int* f = ctx.sm->flag[wg][epoch & 1];
-    bool done = false, v = false;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-        const int a = f[0], b = f[1], c = f[2], d = f[3];
-        if ((a >> 1) >= epoch && (b >> 1) >= epoch && (c >> 1) >= epoch && (d >> 1) >= epoch) {
-            v = ((a | b | c | d) & 1) != 0;
-            done = true;
-            break;
-        }
-        if ((it & 31) == 0 && (ctx.aborted() || globaltimer_ns() - t0 > kWaitLimitNs)) break;
+    return e;
+}
+__device__ __forceinline__ bool group_wait(const Ctx& ctx, int g, int e, bool* any) {
+    const bool ok = ctx.wait_warp(&ctx.sm->gbar[g], e & 1);
+    if (any) {
+        const volatile int* f = ctx.sm->gvote[g][e & 1];
+        *any = ok && (f[0] | f[1] | f[2] | f[3]) != 0;
     }
-    __threadfence_block();
-    if (!done) {
-        *reinterpret_cast<volatile int*>(&ctx.sm->abort) = 1;
-        atomicOr(ctx.status, DFLASH_FLAG_KERNEL_TIMEOUT);
-    }
-    if (any) *any = v;
-    return __all_sync(0xffffffffu, done);
+    return ok;
+}
+__device__ __forceinline__ bool group_sync(const Ctx& ctx, int g, int wq, int& epoch, bool vote,
+                                           bool* any) {
+    return group_wait(ctx, g, group_arrive(ctx, g, wq, epoch, vote), any);
 }
 
 // Source row in the page pool of the 16-key chunk starting at key j0 of sequence b: read from the
@@ -243,6 +248,87 @@ __device__ __forceinline__ void load_terms16(uint32_t taddr, float (&y)[kGroupRo
     for (int i = 0; i < 16; ++i) y[i] = fmaf(f32(a[i]), 0.00390625f, y[i]);
 }
 
+// Grid-wide barrier of one launch (thread 0 of every CTA) on a 64-bit ticket counter: CTA tickets
+// of one launch fall in one block of 2^20 values, the barrier opens when the counter reaches the
+// block base + the CTA count, and the last arrival moves the counter to the next block (so plans
+// of any grid size can share a workspace). One atomic per CTA and no reset on the critical path.
+// Bounded: on timeout the status word gets DFLASH_FLAG_KERNEL_TIMEOUT and false is returned (the
+// counter is then off until the caller zeroes the workspace header). Every CTA must be resident,
+// which the cooperative launch guarantees.
+__device__ __forceinline__ bool grid_barrier(unsigned long long* ctr, uint32_t num_ctas,
+                                             int32_t* status) {
+    constexpr unsigned long long kBlock = 1ull << 20;
+    __threadfence();  // this CTA's split state is written before it arrives
+    const unsigned long long t = atomicAdd(ctr, 1ull);
+    const unsigned long long base = t & ~(kBlock - 1);
+    if (t - base == num_ctas - 1) {  // last arrival: every state is written
+        atomicAdd(ctr, kBlock - num_ctas);
+        __threadfence();
+        return true;
+    }
+    const unsigned long long target = base + num_ctas;
+    const volatile unsigned long long* vctr = ctr;
+    const uint64_t t0 = globaltimer_ns();
+    while (*vctr < target) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(status, DFLASH_FLAG_KERNEL_TIMEOUT);
+            return false;
+        }
+        __nanosleep(32);
+    }
+    __threadfence();
+    return true;
+}
+
+// The merge of a fused launch: once every CTA has written its split state, the CTAs share the
+// (query row, head-dim quarter, sequence x KV head) items of the combine, 256 threads per item
+// (each 256-thread half of the CTA has its own named barrier and scratch at the base of the
+// CTA's shared memory, unused by then).
+template <int NT>
+__device__ __forceinline__ void fused_merge(const PartialParams& p, uint8_t* smem) {
+    constexpr int kHalves = NT / kCombineThreads;
+    constexpr int kQuarters = kHeadDim / (4 * kCombineCols);
+    volatile int* barrier_ok = reinterpret_cast<volatile int*>(smem + kHalves * sizeof(CombineScratch));
+    const int half = threadIdx.x / kCombineThreads;
+    const int cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    const int workers = gridDim.x * gridDim.y * gridDim.z * kHalves;
+    const int items = p.batch * p.num_kv_heads * p.rows * kQuarters;
+    // the context length of this worker's first item is loaded while the barrier is pending
+    const int first = cta * kHalves + half;
+    const int n_first =
+        (half < kHalves && first < items) ? p.context_lens[first / (kQuarters * p.rows) /
+                                                           p.num_kv_heads] : 0;
+    __syncthreads();
+    if (threadIdx.x == 0)
+        *barrier_ok = grid_barrier(p.grid_bar, gridDim.x * gridDim.y * gridDim.z, p.status);
+    __syncthreads();
+    if (!*barrier_ok) return;
+    if (half >= kHalves) return;
+    CombineParams c;
+    c.ws_state = p.ws_state;
+    c.ws_acc = p.ws_acc;
+    c.context_lens = p.context_lens;
+    c.out = p.out;
+    c.lse = p.lse;
+    c.batch = p.batch;
+    c.q_len = p.q_len;
+    c.num_q_heads = p.num_q_heads;
+    c.num_kv_heads = p.num_kv_heads;
+    c.group = p.group;
+    c.rows = p.rows;
+    c.max_context = p.max_context;
+    c.num_splits = p.num_splits;
+    c.tile_keys = p.tile_keys;
+    c.min_split_keys = p.min_split_keys;
+    CombineScratch& sh = reinterpret_cast<CombineScratch*>(smem)[half];
+    for (int it = first; it < items; it += workers) {
+        const int quarter = it % kQuarters, r = (it / kQuarters) % p.rows;
+        const int unit = it / (kQuarters * p.rows);
+        combine_item(c, r, quarter, unit / p.num_kv_heads, unit % p.num_kv_heads,
+                     threadIdx.x % kCombineThreads, 1 + half, sh, it == first ? n_first : -1);
+    }
+}
+
 template <int RP>
 __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     tc_partial_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -263,7 +349,10 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     }
     const int per = keys_per_split(n, p.num_splits, p.tile_keys, p.min_split_keys);
     const int start = split * per;
-    if (start >= n) return;  // idle split: the combine never reads it
+    if (start >= n) {  // idle split: the combine never reads it
+        if (p.out) fused_merge<C::kThreads>(p, smem);
+        return;
+    }
     const int end = min(n, start + per);
     const int ntiles = (end - start + kTile - 1) / kTile;
     const int nvst = (end - start + kVKeys - 1) / kVKeys;
@@ -277,15 +366,12 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     // first copies are already in flight) ------------------------------------------------------
     if (tid == 0) {
         for (int i = 0; i < kKStages; ++i) {
-            mbar_init(smem_u32(&sm.kfull[i]), 1);
+            mbar_init(smem_u32(&sm.kfull[i]), 2);  // one arrival per K-copying warp
             mbar_init(smem_u32(&sm.kempty[i]), 1);
         }
         mbar_init(smem_u32(&sm.sfull), 1);
         mbar_init(smem_u32(&sm.sempty), C::kSoftWarps);
-        for (int i = 0; i < kPStages; ++i) {
-            mbar_init(smem_u32(&sm.pfull[i]), C::kSoftWarps);
-            mbar_init(smem_u32(&sm.pempty[i]), 1);
-        }
+        for (int i = 0; i < kSlices; ++i) mbar_init(smem_u32(&sm.pslice[i]), C::kGroups);
         for (int i = 0; i < kVStages; ++i) {
             mbar_init(smem_u32(&sm.vfull[i]), 1);
             mbar_init(smem_u32(&sm.vfree[i]), 1);
@@ -293,9 +379,12 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         mbar_init(smem_u32(&sm.vtail), 1);
         mbar_init(smem_u32(&sm.odone), 1);
         mbar_init(smem_u32(&sm.qready), C::kSoftWarps);
+        for (int i = 0; i < C::kGroups; ++i) mbar_init(smem_u32(&sm.gbar[i]), 4);
         sm.abort = 0;
-        for (int i = 0; i < (int)(sizeof(sm.flag) / sizeof(int)); ++i) (&sm.flag[0][0][0])[i] = 0;
         fence_mbar_init();
+        // The first K tiles and V stages are copied right away, their pages looked up straight in
+        // the block table (the split's row cache is filled meanwhile by the other threads): the
+        // first copies are the CTA's longest wait. All lookups are in flight together.
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&sm.tmem_base), C::kTmemCols);
@@ -318,19 +407,23 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
-    if (warp == 0) {
-        // ---------------------------------------------------------------- K copies (TMA)
+    if (warp == 0 || warp == 3) {
+        // ------------------------------------------------- K copies (TMA), split over two warps
+        // warp 0 copies the first half of every tile's 16-key chunks, warp 3 the second half;
+        // each arrives once on the tile's barrier with the bytes of its own copies
         if (lane == 0) {
+            constexpr int kHalfChunks = kTile / kChunk / 2;
+            const int c0 = warp == 0 ? 0 : kHalfChunks;
             bool clamped = false;
             int kdone = 0;
             for (int t = 0; t < ntiles; ++t) {
                 const int s = t % kKStages;
                 const int tile0 = start + t * kTile;
-                int rows[kTile / kChunk];
+                int rows[kHalfChunks];
                 int nval = 0;
 #pragma unroll
-                for (int c = 0; c < kTile / kChunk; ++c) {
-                    const int j0 = tile0 + kChunk * c;
+                for (int c = 0; c < kHalfChunks; ++c) {
+                    const int j0 = tile0 + kChunk * (c0 + c);
                     rows[c] = -1;
                     if (j0 < end) {
                         rows[c] = chunk_row(p, sm, b, start, j0, &clamped);
@@ -339,9 +432,9 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                 }
                 if (!ctx.wait(&sm.kempty[s], ((t / kKStages) & 1) ^ 1)) break;
                 mbar_arrive_expect_tx(smem_u32(&sm.kfull[s]), nval * kChunk * kHeadDim);
-                const uint32_t dst = smem_u32(smem + C::kOffK + s * kKStage);
+                const uint32_t dst = smem_u32(smem + C::kOffK + s * kKStage) + c0 * 2048;
 #pragma unroll
-                for (int c = 0; c < kTile / kChunk; ++c) {
+                for (int c = 0; c < kHalfChunks; ++c) {
                     if (rows[c] < 0) continue;
                     tma_load_2d(dst + c * 2048, &kmap, h * kHeadDim, rows[c],
                                 smem_u32(&sm.kfull[s]));
@@ -358,70 +451,87 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
+        // One thread, one event loop over two streams: QK of tile tq (its K copies landed and the
+        // softmax has read the previous scores) and PV of V stage up (its copies and the P slices
+        // it consumes are written). Polling both without blocking keeps a QK from queueing behind
+        // a PV whose V copies are late, and vice versa.
         if (lane == 0 && ctx.wait(&sm.qready, 0)) {
             const uint32_t idesc_qk = idesc_f32acc(128, SN, 0, 0, 0, 0);
             const uint32_t idesc_pv = idesc_f32acc(128, SN, 0, 0, 1, 1);
             const uint32_t q_base = smem_u32(smem + C::kOffQ);
-            // S^T = K Q^T for tile t into the single S buffer (free once the softmax has read
-            // tile t-1's scores)
-            auto issue_qk = [&](int t) -> bool {
-                const int s = t % kKStages;
-                if (!ctx.wait(&sm.kfull[s], (t / kKStages) & 1)) return false;
-                if (!ctx.wait(&sm.sempty, (t & 1) ^ 1)) return false;
-                tc_fence_after();
-                const uint32_t kb = smem_u32(smem + C::kOffK + s * kKStage);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t ad =
-                        smem_desc(kb + (kk >> 2) * kKHalf + (kk & 3) * 32, 16, 1024, kSwizzle128B);
-                    const uint64_t bd = smem_desc(q_base + (kk >> 2) * (SN * 128) + (kk & 3) * 32,
-                                                  16, 1024, kSwizzle128B);
-                    mma_f8_ss(tmem + C::kColS, ad, bd, idesc_qk, kk > 0);
-                }
-                mma_commit(smem_u32(&sm.kempty[s]));
-                mma_commit(smem_u32(&sm.sfull));
-                return true;
-            };
-            // O^T += V^T P^T for tile t: two V stages of 64 keys, two 32-key steps each, both
-            // head-dim halves
-            auto issue_pv = [&](int t) -> bool {
-                const int pb = t % kPStages;
-                if (!ctx.wait(&sm.pfull[pb], (t / kPStages) & 1)) return false;
-                tc_fence_after();
-                const uint32_t pbase = smem_u32(smem + C::kOffP + pb * C::kPStage);
-#pragma unroll 1
-                for (int hv = 0; hv < kTile / kVKeys; ++hv) {
-                    const int u = (kTile / kVKeys) * t + hv;
-                    if (u >= nvst) break;
-                    const int vs = u % kVStages;
-                    if (!ctx.wait(&sm.vfull[vs], (u / kVStages) & 1)) return false;
+            const uint32_t pbase = smem_u32(smem + C::kOffP);
+            constexpr int kStagesPerTile = kTile / kVKeys;
+            int tq = 0, up = 0;
+            uint64_t last = globaltimer_ns();
+            uint32_t idle = 0;
+            while (tq < ntiles || up < nvst) {
+                bool progressed = false;
+                if (tq < ntiles && mbar_test_wait(smem_u32(&sm.kfull[tq % kKStages]),
+                                                  (tq / kKStages) & 1) &&
+                    mbar_test_wait(smem_u32(&sm.sempty), (tq & 1) ^ 1)) {
+                    // S^T = K Q^T into the single S buffer
                     tc_fence_after();
-                    const uint32_t vb = smem_u32(smem + C::kOffV + vs * kVStage);
+                    const int s = tq % kKStages;
+                    const uint32_t kb = smem_u32(smem + C::kOffK + s * kKStage);
 #pragma unroll
-                    for (int kq = 0; kq < kVKeys / 32; ++kq) {
-                        const int kk = (kVKeys / 32) * hv + kq;  // 32-key step within the tile
-                        const uint64_t bd = smem_desc(pbase + kk * 512, 128, 2048, kSwizzleNone);
-#pragma unroll
-                        for (int dh = 0; dh < 2; ++dh) {
-                            const uint64_t ad = smem_desc(vb + dh * kVHalf + kq * 4096, kVHalf,
-                                                          1024, kSwizzle128B);
-                            mma_f8_ss(tmem + C::kColO + dh * SN, ad, bd, idesc_pv, (t | kk) != 0);
-                        }
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t ad = smem_desc(kb + (kk >> 2) * kKHalf + (kk & 3) * 32, 16,
+                                                      1024, kSwizzle128B);
+                        const uint64_t bd = smem_desc(
+                            q_base + (kk >> 2) * (SN * 128) + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+                        mma_f8_ss(tmem + C::kColS, ad, bd, idesc_qk, kk > 0);
                     }
-                    mma_commit(smem_u32(&sm.vfree[vs]));
+                    mma_commit(smem_u32(&sm.kempty[s]));
+                    mma_commit(smem_u32(&sm.sfull));
+                    ++tq;
+                    progressed = true;
                 }
-                mma_commit(smem_u32(&sm.pempty[pb]));
-                return true;
-            };
-            bool ok = issue_qk(0);
-            for (int t = 0; ok && t < ntiles; ++t) {
-                if (t + 1 < ntiles) ok = issue_qk(t + 1);
-                if (ok) ok = issue_pv(t);
+                if (up < nvst) {
+                    const int t = up / kStagesPerTile, hv = up % kStagesPerTile;
+                    const int vs = up % kVStages;
+                    bool ready = mbar_test_wait(smem_u32(&sm.vfull[vs]), (up / kVStages) & 1);
+#pragma unroll
+                    for (int q = 0; q < kSlicesPerStage; ++q)
+                        ready = ready && mbar_test_wait(
+                                             smem_u32(&sm.pslice[kSlicesPerStage * hv + q]), t & 1);
+                    if (ready) {
+                        // O^T += V^T P^T over this stage's keys, both head-dim halves
+                        tc_fence_after();
+                        const uint32_t vb = smem_u32(smem + C::kOffV + vs * kVStage);
+#pragma unroll
+                        for (int kq = 0; kq < kSlicesPerStage; ++kq) {
+                            const int kk = kSlicesPerStage * hv + kq;  // 32-key step of the tile
+                            const uint64_t bd =
+                                smem_desc(pbase + kk * 512, 128, 2048, kSwizzleNone);
+#pragma unroll
+                            for (int dh = 0; dh < 2; ++dh) {
+                                const uint64_t ad = smem_desc(vb + dh * kVHalf + kq * 4096, 4096,
+                                                              1024, kSwizzle128B);
+                                mma_f8_ss(tmem + C::kColO + dh * SN, ad, bd, idesc_pv,
+                                          (t | kk) != 0);
+                            }
+                        }
+                        mma_commit(smem_u32(&sm.vfree[vs]));  // V stage and P slices reusable
+                        ++up;
+                        progressed = true;
+                    }
+                }
+                if (progressed) {
+                    idle = 0;
+                    last = globaltimer_ns();
+                } else if ((++idle & 15) == 0) {
+                    if (ctx.aborted()) break;
+                    if (globaltimer_ns() - last > kWaitLimitNs) {
+                        *reinterpret_cast<volatile int*>(&sm.abort) = 1;
+                        atomicOr(p.status, DFLASH_FLAG_KERNEL_TIMEOUT);
+                        break;
+                    }
+                }
             }
         }
         if (lane == 0) mma_commit(smem_u32(&sm.odone));  // tracks every MMA issued above
     } else if (warp == 2) {
-        // ------------------------------------------- V copies (TMA): 64-key stages, whole warp
+        // ------------------------------------------- V copies (TMA): 32-key stages, whole warp
         bool clamped = false;
         int vdone = 0;
         bool tail_pending = false;  // the ragged last stage's copies are issued but not awaited
@@ -568,17 +678,21 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         }
         int epoch = 0;
         bool alive = ctx.wait_warp(&sm.qready, 0);
-        // per-row scale and minus reference max live in shared memory (read as float4 vectors,
-        // identical for every thread of the group); row sums stay in registers
-        float lsum[kGroupRows];
+        // Per-row score scale and s minus the reference max live in shared memory (read as pairs
+        // of 64-bit words, identical for every thread of the group). Scores, exponents, row sums
+        // and probabilities are handled as FP32 pairs (element i of a 16-row block is word i / 2,
+        // half i % 2).
+        uint64_t lsum[kGroupRows / 2];
         uint32_t rowmask = 0;
 #pragma unroll
-        for (int i = 0; i < kGroupRows; ++i) {
-            lsum[i] = 0.f;
-            rowmask |= (uint32_t)(row0 + i < R) << i;
-        }
-        const float4* c0v = reinterpret_cast<const float4*>(sm.c0 + row0);
-        const float4* negmv = reinterpret_cast<const float4*>(sm.negm + row0);
+        for (int i = 0; i < kGroupRows; ++i) rowmask |= (uint32_t)(row0 + i < R) << i;
+#pragma unroll
+        for (int i = 0; i < kGroupRows / 2; ++i) lsum[i] = 0;
+        const ulonglong2* c0v = reinterpret_cast<const ulonglong2*>(sm.c0 + row0);
+        const ulonglong2* negmv = reinterpret_cast<const ulonglong2*>(sm.negm + row0);
+        const uint64_t k16th = pk2(0.0625f, 0.0625f), k256th = pk2(0.00390625f, 0.00390625f);
+        const uint64_t k16 = pk2(16.f, 16.f);
+        constexpr uint64_t kTrunc4 = 0xFFF00000FFF00000ull;  // sign, exponent, 3 mantissa bits
         for (int t = 0; alive && t < ntiles; ++t) {
             const int tile0 = start + t * kTile;
             const int j = tile0 + st;
@@ -587,9 +701,23 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                 break;
             }
             tc_fence_after();
-            // y = S0 + S1/16 + S2/256: the raw score in MMA units, kept in registers
-            float y[kGroupRows];
-            load_terms16<RP>(lane_base + C::kColS + row0, y);
+            // y = (S0 + S1/16 + S2/256) * c0: the score in log2 units
+            uint64_t y[kGroupRows / 2];
+            {
+                uint32_t a0[16], a1[16], a2[16];
+                const uint32_t sbase = lane_base + C::kColS + row0;
+                tmem_ld16(sbase, a0);
+                tmem_ld16(sbase + RP, a1);
+                tmem_ld16(sbase + 2 * RP, a2);
+                tmem_ld_wait(a0);
+                tmem_ld_wait(a1);
+                tmem_ld_wait(a2);
+#pragma unroll
+                for (int q = 0; q < kGroupRows / 2; ++q)
+                    y[q] = fma2(pk2(f32(a2[2 * q]), f32(a2[2 * q + 1])), k256th,
+                                fma2(pk2(f32(a1[2 * q]), f32(a1[2 * q + 1])), k16th,
+                                     pk2(f32(a0[2 * q]), f32(a0[2 * q + 1]))));
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sm.sempty));  // S free for QK(t+1)
@@ -601,61 +729,110 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                     if (!v) validm &= ~(1u << i);
                 }
             }
-            // y <- score in log2 units; would any visible shifted probability 2^(y + negm) exceed
-            // 2^8?
+            // e = y + (s - m): the exponent of the shifted probability; would any visible one
+            // exceed 2^8?
+            uint64_t e[kGroupRows / 2];
             bool need = false;
 #pragma unroll
             for (int i4 = 0; i4 < kGroupRows / 4; ++i4) {
-                const float4 c = c0v[i4], nm = negmv[i4];
-                y[4 * i4 + 0] *= c.x;
-                y[4 * i4 + 1] *= c.y;
-                y[4 * i4 + 2] *= c.z;
-                y[4 * i4 + 3] *= c.w;
-                need |= ((validm >> (4 * i4 + 0)) & 1u) && y[4 * i4 + 0] + nm.x > kLazyThreshold;
-                need |= ((validm >> (4 * i4 + 1)) & 1u) && y[4 * i4 + 1] + nm.y > kLazyThreshold;
-                need |= ((validm >> (4 * i4 + 2)) & 1u) && y[4 * i4 + 2] + nm.z > kLazyThreshold;
-                need |= ((validm >> (4 * i4 + 3)) & 1u) && y[4 * i4 + 3] + nm.w > kLazyThreshold;
+                const ulonglong2 c = c0v[i4], nm = negmv[i4];
+                y[2 * i4] = mul2(y[2 * i4], c.x);
+                y[2 * i4 + 1] = mul2(y[2 * i4 + 1], c.y);
+                e[2 * i4] = add2(y[2 * i4], nm.x);
+                e[2 * i4 + 1] = add2(y[2 * i4 + 1], nm.y);
             }
+#pragma unroll
+            for (int q = 0; q < kGroupRows / 2; ++q) {
+                need |= ((validm >> (2 * q)) & 1u) && lo2(e[q]) > kLazyThreshold;
+                need |= ((validm >> (2 * q + 1)) & 1u) && hi2(e[q]) > kLazyThreshold;
+            }
+            // shifted probabilities -> three E4M3 terms (this thread's 16 rows of each term are one
+            // 16-byte chunk of P); row sums take the unrounded values
+            uint64_t pv[kGroupRows / 2];
+            uint32_t code[kTerms][4];
+            auto make_p = [&]() {
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    uint32_t ch[2], cm[2], cl[2];
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const int jj = 2 * w + q;
+                        const float p0 = ((validm >> (2 * jj)) & 1u) ? ex2(lo2(e[jj])) : 0.f;
+                        const float p1 = ((validm >> (2 * jj + 1)) & 1u) ? ex2(hi2(e[jj])) : 0.f;
+                        pv[jj] = pk2(p0, p1);
+                        // h, m: truncations to 4 significant bits (mantissa masked), so p - h and
+                        // r - m are exact and the three terms sum to p up to l's final rounding
+                        const uint64_t hv = pv[jj] & kTrunc4;
+                        const uint64_t r = mul2(sub2(pv[jj], hv), k16);
+                        const uint64_t mv = r & kTrunc4;
+                        const uint64_t lv = mul2(sub2(r, mv), k16);
+                        ch[q] = f32x2_to_e4m3x2(hv);
+                        cm[q] = f32x2_to_e4m3x2(mv);
+                        cl[q] = f32x2_to_e4m3x2(lv);
+                    }
+                    code[0][w] = ch[0] | (ch[1] << 16);
+                    code[1][w] = cm[0] | (cm[1] << 16);
+                    code[2][w] = cl[0] | (cl[1] << 16);
+                }
+            };
             bool need_any = false;
-            if (!wg_sync(ctx, g, wq, epoch, __any_sync(0xffffffffu, need), &need_any)) {
+            if (!group_sync(ctx, g, wq, epoch, __any_sync(0xffffffffu, need), &need_any)) {
                 alive = false;
                 break;
             }
+            if (!need_any) make_p();
             bool ok = true;
             if (need_any) {
                 // exact tile maximum per row -> new reference max; rescale row sums and O
 #pragma unroll
-                for (int i = 0; i < kGroupRows; ++i) {
-                    const float m = warp_max(((validm >> i) & 1u) ? y[i] : -INFINITY);
-                    if (lane == 0) sm.red[g][wq][i] = m;
+                for (int q = 0; q < kGroupRows / 2; ++q) {
+                    const float m0 = warp_max(((validm >> (2 * q)) & 1u) ? lo2(y[q]) : -INFINITY);
+                    const float m1 =
+                        warp_max(((validm >> (2 * q + 1)) & 1u) ? hi2(y[q]) : -INFINITY);
+                    if (lane == 0) {
+                        sm.red[g][wq][2 * q] = m0;
+                        sm.red[g][wq][2 * q + 1] = m1;
+                    }
                 }
-                ok = wg_sync(ctx, g, wq, epoch, false, nullptr);
+                ok = group_sync(ctx, g, wq, epoch, false, nullptr);
                 float mnew_own = 0.f;
                 bool own = false;
                 if (ok) {
+                    float alpha[kGroupRows];
 #pragma unroll
                     for (int i = 0; i < kGroupRows; ++i) {
                         const float mo = kPShift - sm.negm[row0 + i];
                         const float tm = fmaxf(fmaxf(sm.red[g][0][i], sm.red[g][1][i]),
                                                fmaxf(sm.red[g][2][i], sm.red[g][3][i]));
                         const float mn = fmaxf(mo, tm);
-                        const float alpha = (mn == -INFINITY) ? 1.f : ex2(mo - mn);
-                        lsum[i] *= alpha;
+                        alpha[i] = (mn == -INFINITY) ? 1.f : ex2(mo - mn);
                         if (i == st) {
-                            sm.alpha[row0 + i] = alpha;
+                            sm.alpha[row0 + i] = alpha[i];
                             mnew_own = mn;
                             own = true;
                         }
                     }
-                    ok = wg_sync(ctx, g, wq, epoch, false, nullptr);  // alphas visible, old m read
+#pragma unroll
+                    for (int q = 0; q < kGroupRows / 2; ++q)
+                        lsum[q] = mul2(lsum[q], pk2(alpha[2 * q], alpha[2 * q + 1]));
+                    ok = group_sync(ctx, g, wq, epoch, false, nullptr);  // alphas visible, old m read
                     if (own) sm.negm[row0 + st] = kPShift - mnew_own;
-                    ok = ok && wg_sync(ctx, g, wq, epoch, false, nullptr);  // new m visible
+                    __threadfence_block();
+                    ok = ok && group_sync(ctx, g, wq, epoch, false, nullptr);  // new m visible
                 }
+#pragma unroll
+                for (int i4 = 0; i4 < kGroupRows / 4; ++i4) {
+                    const ulonglong2 nm = negmv[i4];
+                    e[2 * i4] = add2(y[2 * i4], nm.x);
+                    e[2 * i4 + 1] = add2(y[2 * i4 + 1], nm.y);
+                }
+                make_p();
                 if (ok && t > 0) {
-                    // O holds tiles < t: wait for their PV, then scale this group's row columns
-                    // of all three terms in both head-dim halves
-                    ok = ctx.wait_warp(&sm.pempty[(t - 1) % kPStages],
-                                       ((t - 1) / kPStages) & 1);
+                    // O holds tiles < t: wait for their PV (MMAs complete in issue order, so
+                    // the last V stage of tile t-1 done means all of it), then scale this
+                    // group's row columns of all three terms in both head-dim halves
+                    const int ul = (kTile / kVKeys) * t - 1;
+                    ok = ctx.wait_warp(&sm.vfree[ul % kVStages], (ul / kVStages) & 1);
                     if (ok) {
                         tc_fence_after();
 #pragma unroll 1
@@ -675,33 +852,19 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                     }
                 }
             }
-            // pass 2: probabilities -> three E4M3 terms in P (this thread's 16 rows of each term
-            // are one 16-byte chunk), row sums from the unrounded values
-            const int ps = t % kPStages;
-            if (ok) ok = ctx.wait_warp(&sm.pempty[ps], ((t / kPStages) & 1) ^ 1);
+#pragma unroll
+            for (int q = 0; q < kGroupRows / 2; ++q) lsum[q] = add2(lsum[q], pv[q]);
+            // P slice wq (this warp's keys) is free once the V stage that consumed it in tile t-1
+            // is done
+            if (ok && t > 0) {
+                const int u = (kTile / kVKeys) * (t - 1) + wq / kSlicesPerStage;
+                ok = ctx.wait_warp(&sm.vfree[u % kVStages], (u / kVStages) & 1);
+            }
             if (!ok) {
                 alive = false;
                 break;
             }
-            uint32_t code[kTerms][4];
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const float4 nm = negmv[w];
-                float pv[4];
-                pv[0] = ((validm >> (4 * w + 0)) & 1u) ? ex2(y[4 * w + 0] + nm.x) : 0.f;
-                pv[1] = ((validm >> (4 * w + 1)) & 1u) ? ex2(y[4 * w + 1] + nm.y) : 0.f;
-                pv[2] = ((validm >> (4 * w + 2)) & 1u) ? ex2(y[4 * w + 2] + nm.z) : 0.f;
-                pv[3] = ((validm >> (4 * w + 3)) & 1u) ? ex2(y[4 * w + 3] + nm.w) : 0.f;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) lsum[4 * w + e] += pv[e];
-                uint32_t h01, m01, l01, h23, m23, l23;
-                split3_x2(pv[0], pv[1], h01, m01, l01);
-                split3_x2(pv[2], pv[3], h23, m23, l23);
-                code[0][w] = h01 | (h23 << 16);
-                code[1][w] = m01 | (m23 << 16);
-                code[2][w] = l01 | (l23 << 16);
-            }
-            uint8_t* pbuf = smem + C::kOffP + ps * C::kPStage;
+            uint8_t* pbuf = smem + C::kOffP;
 #pragma unroll
             for (int term = 0; term < kTerms; ++term)
                 *reinterpret_cast<uint4*>(pbuf + p_chunk(term * C::kGroups + g, st)) =
@@ -709,15 +872,18 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             fence_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sm.pfull[ps]));
+            if (lane == 0) mbar_arrive(smem_u32(&sm.pslice[wq]));
         }
         // row sums over the 128 key lanes -> split state (max m - s, shifted sums and numerator)
 #pragma unroll
-        for (int i = 0; i < kGroupRows; ++i) {
-            const float v = warp_sum(lsum[i]);
-            if (lane == 0) sm.red[g][wq][i] = v;
+        for (int q = 0; q < kGroupRows / 2; ++q) {
+            const float v0 = warp_sum(lo2(lsum[q])), v1 = warp_sum(hi2(lsum[q]));
+            if (lane == 0) {
+                sm.red[g][wq][2 * q] = v0;
+                sm.red[g][wq][2 * q + 1] = v1;
+            }
         }
-        if (alive) alive = wg_sync(ctx, g, wq, epoch, false, nullptr);
+        if (alive) alive = group_sync(ctx, g, wq, epoch, false, nullptr);
         const int64_t unit = ((int64_t)b * p.num_kv_heads + h) * p.num_splits + split;
         if (alive && !ctx.aborted()) {
 #pragma unroll
@@ -754,6 +920,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
+    if (p.out) fused_merge<C::kThreads>(p, smem);
 }
 
 }  // namespace tc
@@ -803,9 +970,19 @@ static cudaError_t launch_rp(const CUtensorMap& kmap, const CUtensorMap& vmap,
     cudaError_t e = cudaFuncSetAttribute(tc::tc_partial_kernel<RP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.num_splits, p.num_kv_heads, p.batch);
-    tc::tc_partial_kernel<RP><<<grid, tc::Cfg<RP>::kThreads, smem, stream>>>(kmap, vmap, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.num_splits, p.num_kv_heads, p.batch);
+    cfg.blockDim = dim3(tc::Cfg<RP>::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (p.out) {  // the fused merge waits for every CTA: they must all be resident at once
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, tc::tc_partial_kernel<RP>, kmap, vmap, p);
 }
 
 cudaError_t launch_tc_partial(const PartialParams& p, cudaStream_t stream) {

@@ -50,6 +50,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Non-blocking test: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Wait for the phase with the given parity to complete. Gives up (returns false) when *abort
 // becomes non-zero or after limit_ns nanoseconds, so no wait can spin forever.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
@@ -98,6 +110,56 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
     uint16_t out;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(out) : "f"(hi), "f"(lo));
+    return out;
+}
+
+// ---- packed FP32 pairs (f32x2 arithmetic of sm_100 and later: one instruction, two lanes) -----
+// A pair lives in a 64-bit register (low word = first element). Only used where every result is
+// exact or where the rounding does not matter: on this GPU the code generator may evaluate
+// chains of these operations without rounding each step (a Veltkamp split c - (c - x) with
+// c = x(2^20 + 1) came back as x), so they must not carry error-free-transformation tricks.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float lo2(uint64_t x) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+    return lo;
+}
+__device__ __forceinline__ float hi2(uint64_t x) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+    return hi;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// A pair -> two E4M3FN codes (first element in the low byte), round to nearest even, saturated.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(uint64_t x) {
+    uint16_t out;
+    asm("{\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 %0, hi, lo;\n\t}"
+        : "=h"(out)
+        : "l"(x));
     return out;
 }
 

@@ -37,7 +37,7 @@ def algorithmic_bytes(w: W.Workload, plan) -> dict:
 
 class LayerStack:
     def __init__(self, w: W.Workload, device="cuda", num_splits=0, kernel=B.DFLASH_KERNEL_AUTO,
-                 layers=None):
+                 layers=None, flags=0):
         self.w = w
         self.device = torch.device(device)
         n_layers = w.layers if layers is None else layers
@@ -45,7 +45,7 @@ class LayerStack:
         self.att = B.VerifyAttention(w.batch, w.q_len, w.num_q_heads, w.num_kv_heads,
                                      w.head_dim, w.page_size, w.max_pages_per_seq, w.num_pages,
                                      w.max_ctx, device=self.device.index or 0,
-                                     num_splits=num_splits, kernel=kernel)
+                                     num_splits=num_splits, kernel=kernel, flags=flags)
         shape = (w.batch, w.q_len, w.num_q_heads, w.head_dim)
         self.outs = [torch.empty(shape, dtype=torch.float16, device=self.device)
                      for _ in self.layers]

@@ -58,8 +58,24 @@ def to_device(inputs, device="cuda"):
     return {k: v.to(device) for k, v in inputs.items()}
 
 
+# Kernel modes of the parity tests: the CUDA-core kernel, the tensor-core kernel with the combine
+# kernel (the default forward), and the tensor-core kernel with the splits merged inside the same
+# cooperative launch.
+SIMT, TCGEN05, TCGEN05_FUSED = 1, 2, 3
+MODES = [SIMT, TCGEN05, TCGEN05_FUSED]
+
+
+def kernel_args(mode):
+    """VerifyAttention keyword arguments of a test mode."""
+    from speculative_verify_paged_e4m3_gb300 import binding as B
+    if mode == TCGEN05_FUSED:
+        return dict(kernel=B.DFLASH_KERNEL_TCGEN05, flags=B.DFLASH_PROBLEM_FUSED_COMBINE)
+    return dict(kernel=mode, flags=0)
+
+
 def gpu_forward(inputs, num_splits=0, kernel=0, max_context=None, num_pages=None):
-    """Plan for the inputs' shape and run partial + combine on the current stream."""
+    """Plan for the inputs' shape and run partial + combine on the current stream (kernel: a
+    test mode, see MODES, or 0 for the planner's choice)."""
     from speculative_verify_paged_e4m3_gb300 import binding as B
     q = inputs["q"]
     bq, q_len, Hq, D = q.shape
@@ -69,7 +85,7 @@ def gpu_forward(inputs, num_splits=0, kernel=0, max_context=None, num_pages=None
         max_context = max(1, mpps * P)
     att = B.VerifyAttention(bq, q_len, Hq, Hkv, D, P, mpps,
                             num_pool_pages if num_pages is None else num_pages, max_context,
-                            num_splits=num_splits, kernel=kernel)
+                            num_splits=num_splits, **kernel_args(kernel))
     out, lse = att(inputs["q"], inputs["k_pool"], inputs["v_pool"], inputs["block_table"],
                    inputs["context_lens"], inputs["k_scale"], inputs["v_scale"])
     torch.cuda.synchronize()

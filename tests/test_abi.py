@@ -148,3 +148,39 @@ def test_status_strings(B):
     for s in (0, -1, -2, -3, -4):
         assert B.status_string(s)
     assert B.status_string(12345) == "unknown status"
+
+
+def test_fused_combine_planning(B):
+    """On request the tensor-core plan merges the splits in its own launch, when the whole grid
+    fits on the GPU at once (one CTA per SM), and not otherwise; the default is two kernels."""
+    F = B.DFLASH_PROBLEM_FUSED_COMBINE
+    assert B.dflash_verify_attn_plan(problem(B)).combine_fused == 0
+    plan = B.dflash_verify_attn_plan(problem(B, flags=F))
+    assert plan.combine_fused == 1
+    assert plan.num_splits * plan.problem.batch * plan.problem.num_kv_heads <= plan.sm_count
+    simt = B.dflash_verify_attn_plan(problem(B, kernel=B.DFLASH_KERNEL_SIMT, flags=F))
+    assert simt.combine_fused == 0
+    forced = B.dflash_verify_attn_plan(problem(B, num_splits=300, flags=F))
+    assert forced.combine_fused == 0
+    forced_small = B.dflash_verify_attn_plan(problem(B, num_splits=100, flags=F))
+    assert forced_small.combine_fused == 1 and forced_small.num_splits == 100
+    many = B.dflash_verify_attn_plan(problem(B, batch=153, max_pages_per_seq=16, num_pages=4096,
+                                             max_context=256, flags=F))
+    assert many.combine_fused == 0
+    # batch x KV heads units share the SMs: floor(152 / 3) splits each
+    three = B.dflash_verify_attn_plan(problem(B, batch=3, flags=F))
+    assert three.combine_fused == 1 and three.num_splits == 152 // 3
+
+
+def test_fused_forward_rejects_bad_arguments_without_launching(B):
+    plan = B.dflash_verify_attn_plan(problem(B, flags=B.DFLASH_PROBLEM_FUSED_COMBINE))
+    assert plan.combine_fused == 1
+    lib = B.load_library()
+    fake = ctypes.c_void_p(1 << 20)
+    args = [fake] * 8
+    rc = lib.dflash_verify_attn_forward(ctypes.byref(plan), *args, ctypes.c_size_t(plan.workspace_bytes),
+                                        None, fake, None)
+    assert rc == B.DFLASH_ERR_INVALID_ARGUMENT  # no output
+    rc = lib.dflash_verify_attn_forward(ctypes.byref(plan), *args,
+                                        ctypes.c_size_t(plan.workspace_bytes - 1), fake, fake, None)
+    assert rc == B.DFLASH_ERR_WORKSPACE_TOO_SMALL

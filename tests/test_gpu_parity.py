@@ -6,12 +6,13 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import compare, gpu_forward, oracle_forward, to_device, to_np
+from gpu_helpers import (MODES, compare, gpu_forward, kernel_args, oracle_forward, to_device,
+                         to_np)
 from speculative_verify_paged_e4m3_gb300 import workload as W
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = [1, 2]  # DFLASH_KERNEL_SIMT, DFLASH_KERNEL_TCGEN05
+KERNELS = MODES  # CUDA-core; tensor-core + combine kernel; tensor-core fused forward
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -165,10 +166,10 @@ def test_deterministic_and_canaries_intact(kernel):
     Bq, q_len, Hq, D = dev["q"].shape
     guard = 4096
     att = B.VerifyAttention(Bq, q_len, Hq, 1, D, 16, dev["block_table"].shape[1],
-                            dev["k_pool"].shape[0], 3333, kernel=kernel)
+                            dev["k_pool"].shape[0], 3333, **kernel_args(kernel))
     ws_bytes = att.plan.workspace_bytes
     big_ws = torch.full((ws_bytes + 2 * guard,), 0xA5, dtype=torch.uint8, device="cuda")
-    big_ws[guard:guard + 4].zero_()
+    big_ws[guard:guard + 16].zero_()  # status word and grid-barrier words of the header
     att.workspace = big_ws[guard:guard + ws_bytes]
     n_out = Bq * q_len * Hq * D
     out_buf = torch.full((n_out + 2 * guard,), 7.0, dtype=torch.float16, device="cuda")
@@ -205,3 +206,47 @@ def test_debug_dequant_bit_exact():
         sc32 = np.float64(np.float32(sc))
         ref_scaled = (ref[~nan] * sc32).astype(np.float32)  # exact product, one rounding
         assert np.array_equal(to_np(scd)[~nan].view(np.uint32), ref_scaled.view(np.uint32))
+
+
+def test_fused_and_separate_combine_agree_bitwise():
+    """The fused forward runs the same merge arithmetic as the combine kernel: same bits."""
+    from speculative_verify_paged_e4m3_gb300 import binding as B
+    w = small("fused_vs_sep", [5000], seed=71)
+    dev = to_device(W.make_layer(w, 0, device="cpu"))
+    res = []
+    for flags in (B.DFLASH_PROBLEM_FUSED_COMBINE, 0):
+        att = B.VerifyAttention(1, 8, 6, 1, 256, 16, dev["block_table"].shape[1],
+                                dev["k_pool"].shape[0], 5000, num_splits=9,
+                                kernel=B.DFLASH_KERNEL_TCGEN05, flags=flags)
+        assert att.plan.combine_fused == (1 if flags else 0)
+        out, lse = att(dev["q"], dev["k_pool"], dev["v_pool"], dev["block_table"],
+                       dev["context_lens"], dev["k_scale"], dev["v_scale"])
+        torch.cuda.synchronize()
+        res.append((out.clone(), lse.clone()))
+    assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
+
+
+def test_fused_barrier_reused_across_grid_sizes():
+    """One workspace, fused plans of different grid sizes back to back: the grid barrier resets
+    itself, every result matches the oracle and no timeout is flagged."""
+    from speculative_verify_paged_e4m3_gb300 import binding as B
+    w = small("fused_reuse", [2600, 700], seed=81)
+    inp = W.make_layer(w, 0, device="cpu")
+    dev = to_device(inp)
+    ref_out, ref_lse = oracle_forward(inp)
+    ws = None
+    for splits in (0, 37, 5, 76, 1, 0):
+        att = B.VerifyAttention(2, 8, 6, 1, 256, 16, dev["block_table"].shape[1],
+                                dev["k_pool"].shape[0], 2600, num_splits=splits,
+                                kernel=B.DFLASH_KERNEL_TCGEN05,
+                                flags=B.DFLASH_PROBLEM_FUSED_COMBINE)
+        assert att.plan.combine_fused == 1
+        if ws is None or ws.numel() < att.plan.workspace_bytes:
+            big = torch.zeros(1 << 24, dtype=torch.uint8, device="cuda")
+            ws = big
+        att.workspace = ws
+        out, lse = att(dev["q"], dev["k_pool"], dev["v_pool"], dev["block_table"],
+                       dev["context_lens"], dev["k_scale"], dev["v_scale"])
+        torch.cuda.synchronize()
+        compare(to_np(out), to_np(lse), ref_out, ref_lse, what=f"fused splits={splits}")
+        assert att.workspace_views()[0].item() == 0
