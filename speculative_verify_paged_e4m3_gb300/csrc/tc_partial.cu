@@ -114,14 +114,12 @@ struct Small {
     uint32_t tmem_base;
     int abort;
     int gvote[kMaxRP / kGroupRows][2][4];  // group votes: [group][phase parity][warp]
-    alignas(16) float c0[kMaxRP];    // score scale of each row (log2 units per MMA unit), float4 reads
-    alignas(16) float negm[kMaxRP];  // s minus the reference max of each row (+inf: none yet), float4
-    float red[kMaxRP / kGroupRows][4][kGroupRows];  // per-group, per-warp partials (max, row sums)
-    float alpha[kMaxRP];
+    alignas(16) float c0[kMaxRP];  // score scale of each row (log2 units per MMA unit), float4 reads
+    float rmax[kMaxRP / kGroupRows][4][kGroupRows];  // per-group, per-warp row maxima of a tile
+    float rsum[kMaxRP / kGroupRows][4][kGroupRows];  // per-group, per-warp row sums of the split
     int rows[kRowCache];  // source row (physical page * page + slot) of chunk c of the split
 };
-static_assert(offsetof(Small, c0) % 16 == 0 && offsetof(Small, negm) % 16 == 0,
-              "row constants are read as float4");
+static_assert(offsetof(Small, c0) % 16 == 0, "row constants are read as float4");
 
 template <int RP>
 constexpr uint32_t smem_bytes() {
@@ -667,10 +665,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                                               kmajor_off(term * RP + r, lane * 8, SN)) =
                         make_uint2(packed[0], packed[1]);
                 }
-                if (lane == 0) {
-                    sm.c0[r] = qk_scale * __int_as_float((127 - a) << 23);
-                    sm.negm[r] = INFINITY;  // no key seen yet
-                }
+                if (lane == 0) sm.c0[r] = qk_scale * __int_as_float((127 - a) << 23);
             }
             fence_async_smem();
             __syncwarp();
@@ -689,7 +684,11 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kGroupRows / 2; ++i) lsum[i] = 0;
         const ulonglong2* c0v = reinterpret_cast<const ulonglong2*>(sm.c0 + row0);
-        const ulonglong2* negmv = reinterpret_cast<const ulonglong2*>(sm.negm + row0);
+        // s minus the reference max of each of the group's rows (+inf: none yet), in pairs; every
+        // thread of the group holds the same values (they are computed from shared partials)
+        uint64_t nm[kGroupRows / 2];
+#pragma unroll
+        for (int q = 0; q < kGroupRows / 2; ++q) nm[q] = pk2(INFINITY, INFINITY);
         const uint64_t k16th = pk2(0.0625f, 0.0625f), k256th = pk2(0.00390625f, 0.00390625f);
         const uint64_t k16 = pk2(16.f, 16.f);
         constexpr uint64_t kTrunc4 = 0xFFF00000FFF00000ull;  // sign, exponent, 3 mantissa bits
@@ -735,11 +734,11 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             bool need = false;
 #pragma unroll
             for (int i4 = 0; i4 < kGroupRows / 4; ++i4) {
-                const ulonglong2 c = c0v[i4], nm = negmv[i4];
+                const ulonglong2 c = c0v[i4];
                 y[2 * i4] = mul2(y[2 * i4], c.x);
                 y[2 * i4 + 1] = mul2(y[2 * i4 + 1], c.y);
-                e[2 * i4] = add2(y[2 * i4], nm.x);
-                e[2 * i4 + 1] = add2(y[2 * i4 + 1], nm.y);
+                e[2 * i4] = add2(y[2 * i4], nm[2 * i4]);
+                e[2 * i4 + 1] = add2(y[2 * i4 + 1], nm[2 * i4 + 1]);
             }
 #pragma unroll
             for (int q = 0; q < kGroupRows / 2; ++q) {
@@ -775,59 +774,50 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                     code[2][w] = cl[0] | (cl[1] << 16);
                 }
             };
-            bool need_any = false;
-            if (!group_sync(ctx, g, wq, epoch, __any_sync(0xffffffffu, need), &need_any)) {
+            // tile 0 always sets the reference max; later tiles vote on whether to move it
+            bool need_any = true;
+            if (t > 0 &&
+                !group_sync(ctx, g, wq, epoch, __any_sync(0xffffffffu, need), &need_any)) {
                 alive = false;
                 break;
             }
-            if (!need_any) make_p();
             bool ok = true;
             if (need_any) {
-                // exact tile maximum per row -> new reference max; rescale row sums and O
+                // exact tile maximum per row -> new reference max (every thread of the group derives
+                // the same values from the warps' partial maxima); rescale row sums and O
 #pragma unroll
                 for (int q = 0; q < kGroupRows / 2; ++q) {
                     const float m0 = warp_max(((validm >> (2 * q)) & 1u) ? lo2(y[q]) : -INFINITY);
                     const float m1 =
                         warp_max(((validm >> (2 * q + 1)) & 1u) ? hi2(y[q]) : -INFINITY);
                     if (lane == 0) {
-                        sm.red[g][wq][2 * q] = m0;
-                        sm.red[g][wq][2 * q + 1] = m1;
+                        sm.rmax[g][wq][2 * q] = m0;
+                        sm.rmax[g][wq][2 * q + 1] = m1;
                     }
                 }
-                ok = group_sync(ctx, g, wq, epoch, false, nullptr);
-                float mnew_own = 0.f;
-                bool own = false;
-                if (ok) {
-                    float alpha[kGroupRows];
+                if (!group_sync(ctx, g, wq, epoch, false, nullptr)) {
+                    alive = false;
+                    break;
+                }
+                float alpha[kGroupRows];
 #pragma unroll
-                    for (int i = 0; i < kGroupRows; ++i) {
-                        const float mo = kPShift - sm.negm[row0 + i];
-                        const float tm = fmaxf(fmaxf(sm.red[g][0][i], sm.red[g][1][i]),
-                                               fmaxf(sm.red[g][2][i], sm.red[g][3][i]));
+                for (int q = 0; q < kGroupRows / 2; ++q) {
+                    float nmq[2] = {lo2(nm[q]), hi2(nm[q])};
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const int i = 2 * q + k;
+                        const float mo = kPShift - nmq[k];
+                        const float tm = fmaxf(fmaxf(sm.rmax[g][0][i], sm.rmax[g][1][i]),
+                                               fmaxf(sm.rmax[g][2][i], sm.rmax[g][3][i]));
                         const float mn = fmaxf(mo, tm);
                         alpha[i] = (mn == -INFINITY) ? 1.f : ex2(mo - mn);
-                        if (i == st) {
-                            sm.alpha[row0 + i] = alpha[i];
-                            mnew_own = mn;
-                            own = true;
-                        }
+                        nmq[k] = (mn == -INFINITY) ? INFINITY : kPShift - mn;
                     }
-#pragma unroll
-                    for (int q = 0; q < kGroupRows / 2; ++q)
-                        lsum[q] = mul2(lsum[q], pk2(alpha[2 * q], alpha[2 * q + 1]));
-                    ok = group_sync(ctx, g, wq, epoch, false, nullptr);  // alphas visible, old m read
-                    if (own) sm.negm[row0 + st] = kPShift - mnew_own;
-                    __threadfence_block();
-                    ok = ok && group_sync(ctx, g, wq, epoch, false, nullptr);  // new m visible
+                    nm[q] = pk2(nmq[0], nmq[1]);
+                    lsum[q] = mul2(lsum[q], pk2(alpha[2 * q], alpha[2 * q + 1]));
+                    e[q] = add2(y[q], nm[q]);
                 }
-#pragma unroll
-                for (int i4 = 0; i4 < kGroupRows / 4; ++i4) {
-                    const ulonglong2 nm = negmv[i4];
-                    e[2 * i4] = add2(y[2 * i4], nm.x);
-                    e[2 * i4 + 1] = add2(y[2 * i4 + 1], nm.y);
-                }
-                make_p();
-                if (ok && t > 0) {
+                if (t > 0) {
                     // O holds tiles < t: wait for their PV (MMAs complete in issue order, so
                     // the last V stage of tile t-1 done means all of it), then scale this
                     // group's row columns of all three terms in both head-dim halves
@@ -845,13 +835,14 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                             tmem_ld_wait(o);
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
-                                o[i] = __float_as_uint(f32(o[i]) * sm.alpha[row0 + i]);
+                                o[i] = __float_as_uint(f32(o[i]) * alpha[i]);
                             tmem_st16(addr, o);
                         }
                         tmem_st_wait();
                     }
                 }
             }
+            make_p();
 #pragma unroll
             for (int q = 0; q < kGroupRows / 2; ++q) lsum[q] = add2(lsum[q], pv[q]);
             // P slice wq (this warp's keys) is free once the V stage that consumed it in tile t-1
@@ -879,19 +870,24 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         for (int q = 0; q < kGroupRows / 2; ++q) {
             const float v0 = warp_sum(lo2(lsum[q])), v1 = warp_sum(hi2(lsum[q]));
             if (lane == 0) {
-                sm.red[g][wq][2 * q] = v0;
-                sm.red[g][wq][2 * q + 1] = v1;
+                sm.rsum[g][wq][2 * q] = v0;
+                sm.rsum[g][wq][2 * q + 1] = v1;
             }
         }
         if (alive) alive = group_sync(ctx, g, wq, epoch, false, nullptr);
         const int64_t unit = ((int64_t)b * p.num_kv_heads + h) * p.num_splits + split;
         if (alive && !ctx.aborted()) {
 #pragma unroll
-            for (int i = 0; i < kGroupRows; ++i) {
-                if (st == i && row0 + i < R) {
-                    const float L = sm.red[g][0][i] + sm.red[g][1][i] + sm.red[g][2][i] +
-                                    sm.red[g][3][i];
-                    p.ws_state[unit * R + row0 + i] = make_float2(-sm.negm[row0 + i], L);
+            for (int q = 0; q < kGroupRows / 2; ++q) {
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int i = 2 * q + k;
+                    if (st == i && row0 + i < R) {
+                        const float L = sm.rsum[g][0][i] + sm.rsum[g][1][i] + sm.rsum[g][2][i] +
+                                        sm.rsum[g][3][i];
+                        p.ws_state[unit * R + row0 + i] =
+                            make_float2(-(k ? hi2(nm[q]) : lo2(nm[q])), L);
+                    }
                 }
             }
         }
