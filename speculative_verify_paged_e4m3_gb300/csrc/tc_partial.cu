@@ -180,10 +180,19 @@ struct Ctx {
         return false;
     }
     // The same for code run by a whole warp: every lane waits, and the warp agrees on the result,
-    // so that no later warp-synchronous instruction runs with part of the warp gone.
+    // so that no later warp-synchronous instruction runs with part of the warp gone. For waits
+    // after which the lanes read data the async proxy wrote (TMA copies).
     __device__ bool wait_warp(uint64_t* bar, uint32_t parity) const {
         const bool ok = wait(bar, parity);
         return __all_sync(0xffffffffu, ok);
+    }
+    // A whole warp's wait carried out by lane 0 alone, the result broadcast to the warp. For waits
+    // that order a buffer's reuse or precede tensor-memory loads (tcgen05.fence::after_thread_sync
+    // follows).
+    __device__ bool wait_lane0(uint64_t* bar, uint32_t parity) const {
+        bool ok = true;
+        if ((threadIdx.x & 31) == 0) ok = wait(bar, parity);
+        return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     }
     __device__ bool aborted() const { return *reinterpret_cast<volatile int*>(&sm->abort) != 0; }
 };
@@ -364,14 +373,14 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     // first copies are already in flight) ------------------------------------------------------
     if (tid == 0) {
         for (int i = 0; i < kKStages; ++i) {
-            mbar_init(smem_u32(&sm.kfull[i]), 2);  // one arrival per K-copying warp
+            mbar_init(smem_u32(&sm.kfull[i]), 3);  // one arrival per copying warp
             mbar_init(smem_u32(&sm.kempty[i]), 1);
         }
         mbar_init(smem_u32(&sm.sfull), 1);
         mbar_init(smem_u32(&sm.sempty), C::kSoftWarps);
         for (int i = 0; i < kSlices; ++i) mbar_init(smem_u32(&sm.pslice[i]), C::kGroups);
         for (int i = 0; i < kVStages; ++i) {
-            mbar_init(smem_u32(&sm.vfull[i]), 1);
+            mbar_init(smem_u32(&sm.vfull[i]), 3);  // one arrival per copying warp
             mbar_init(smem_u32(&sm.vfree[i]), 1);
         }
         mbar_init(smem_u32(&sm.vtail), 1);
@@ -380,9 +389,6 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         for (int i = 0; i < C::kGroups; ++i) mbar_init(smem_u32(&sm.gbar[i]), 4);
         sm.abort = 0;
         fence_mbar_init();
-        // The first K tiles and V stages are copied right away, their pages looked up straight in
-        // the block table (the split's row cache is filled meanwhile by the other threads): the
-        // first copies are the CTA's longest wait. All lookups are in flight together.
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&sm.tmem_base), C::kTmemCols);
@@ -405,47 +411,167 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
-    if (warp == 0 || warp == 3) {
-        // ------------------------------------------------- K copies (TMA), split over two warps
-        // warp 0 copies the first half of every tile's 16-key chunks, warp 3 the second half;
-        // each arrives once on the tile's barrier with the bytes of its own copies
-        if (lane == 0) {
-            constexpr int kHalfChunks = kTile / kChunk / 2;
-            const int c0 = warp == 0 ? 0 : kHalfChunks;
-            bool clamped = false;
-            int kdone = 0;
-            for (int t = 0; t < ntiles; ++t) {
-                const int s = t % kKStages;
-                const int tile0 = start + t * kTile;
-                int rows[kHalfChunks];
-                int nval = 0;
+    if (warp == 0 || warp == 2 || warp == 3) {
+        // --------------------------------------------------------- K and V copies (TMA)
+        // Three warps share the copies of every tile: one warp's TMA instruction stream issues
+        // about 15 boxes a microsecond, an SM about 22, and a tile takes 32 (16-key chunks, two
+        // 128-byte halves, K and V). Copier ci owns the K chunks c with c % 3 == ci and the V
+        // chunks with c % 3 == (ci + 1) % 3, and arrives once per K tile and per V stage with the
+        // bytes of its own copies. Each copier polls both rings without blocking, K first (the
+        // scores come before the probabilities). A ragged last V stage is copied whole by copier
+        // 1, which zeroes its keys past the split's end once they have landed (P is zero there,
+        // but a stale NaN code times zero is NaN); the others only arrive on it.
+        const int ci = warp == 0 ? 0 : (warp == 2 ? 1 : 2);
+        const uint64_t stream = l2_evict_first_policy();  // every page is read once
+        constexpr int kChunks = kTile / kChunk;          // 8 per K tile and per V stage
+        constexpr int kOwn = (kChunks + 2) / 3;           // at most 3 chunks per copier
+        static_assert(kVKeys == kTile, "one V stage per tile");
+        bool clamped = false;
+        // the pool rows of this copier's chunks of K tile tk and V stage tv, looked up ahead
+        auto own_rows = [&](int tile0, int first, int (&rows)[kOwn]) {
 #pragma unroll
-                for (int c = 0; c < kHalfChunks; ++c) {
-                    const int j0 = tile0 + kChunk * (c0 + c);
-                    rows[c] = -1;
-                    if (j0 < end) {
-                        rows[c] = chunk_row(p, sm, b, start, j0, &clamped);
-                        ++nval;
-                    }
-                }
-                if (!ctx.wait(&sm.kempty[s], ((t / kKStages) & 1) ^ 1)) break;
-                mbar_arrive_expect_tx(smem_u32(&sm.kfull[s]), nval * kChunk * kHeadDim);
-                const uint32_t dst = smem_u32(smem + C::kOffK + s * kKStage) + c0 * 2048;
-#pragma unroll
-                for (int c = 0; c < kHalfChunks; ++c) {
-                    if (rows[c] < 0) continue;
-                    tma_load_2d(dst + c * 2048, &kmap, h * kHeadDim, rows[c],
-                                smem_u32(&sm.kfull[s]));
-                    tma_load_2d(dst + c * 2048 + kKHalf, &kmap, h * kHeadDim + 128, rows[c],
-                                smem_u32(&sm.kfull[s]));
-                }
-                kdone = t + 1;
+            for (int k = 0; k < kOwn; ++k) {
+                const int c = first + 3 * k;
+                const int j0 = tile0 + kChunk * c;
+                rows[k] = (c < kChunks && j0 < end) ? chunk_row(p, sm, b, start, j0, &clamped) : -1;
             }
+        };
+        const int kfirst = ci, vfirst = (ci + 1) % 3;
+        int krows[kOwn], vrows[kOwn];
+        if (lane == 0) {
+            own_rows(start, kfirst, krows);
+            own_rows(start, vfirst, vrows);
+        }
+        int tk = 0, tv = 0;
+        bool tail_pending = false;  // the ragged stage's copies are issued but not awaited
+        uint64_t last = globaltimer_ns();
+        uint32_t idle = 0;
+        while (tk < ntiles || tv < nvst) {
+            bool progressed = false;
+            bool kready = false, vready = false;
+            if (lane == 0) {
+                kready = tk < ntiles && mbar_test_wait(smem_u32(&sm.kempty[tk % kKStages]),
+                                                       ((tk / kKStages) & 1) ^ 1);
+                vready = tv < nvst && mbar_test_wait(smem_u32(&sm.vfree[tv % kVStages]),
+                                                     ((tv / kVStages) & 1) ^ 1);
+            }
+            kready = __shfl_sync(0xffffffffu, kready, 0);
+            vready = __shfl_sync(0xffffffffu, vready, 0);
+            if (kready) {
+                if (lane == 0) {
+                    const int s = tk % kKStages;
+                    const uint32_t bar = smem_u32(&sm.kfull[s]);
+                    int nval = 0;
+#pragma unroll
+                    for (int k = 0; k < kOwn; ++k) nval += krows[k] >= 0;
+                    mbar_arrive_expect_tx(bar, nval * kChunk * kHeadDim);
+                    const uint32_t dst = smem_u32(smem + C::kOffK + s * kKStage);
+#pragma unroll
+                    for (int k = 0; k < kOwn; ++k) {
+                        if (krows[k] < 0) continue;
+                        const uint32_t d = dst + (kfirst + 3 * k) * 2048;
+                        tma_load_2d(d, &kmap, h * kHeadDim, krows[k], bar, stream);
+                        tma_load_2d(d + kKHalf, &kmap, h * kHeadDim + 128, krows[k], bar, stream);
+                    }
+                    if (tk + 1 < ntiles) own_rows(start + (tk + 1) * kTile, kfirst, krows);
+                }
+                ++tk;
+                progressed = true;
+            }
+            if (vready) {
+                const int vs = tv % kVStages;
+                const int h0 = start + tv * kVKeys;
+                const int nkeys = min(kVKeys, end - h0);
+                uint8_t* vstage = smem + C::kOffV + vs * kVStage;
+                if (nkeys == kVKeys) {
+                    if (lane == 0) {
+                        const uint32_t bar = smem_u32(&sm.vfull[vs]);
+                        int nval = 0;
+#pragma unroll
+                        for (int k = 0; k < kOwn; ++k) nval += vrows[k] >= 0;
+                        mbar_arrive_expect_tx(bar, nval * kChunk * kHeadDim);
+                        const uint32_t dst = smem_u32(vstage);
+#pragma unroll
+                        for (int k = 0; k < kOwn; ++k) {
+                            if (vrows[k] < 0) continue;
+                            const uint32_t d = dst + (vfirst + 3 * k) * 2048;
+                            tma_load_2d(d, &vmap, h * kHeadDim, vrows[k], bar, stream);
+                            tma_load_2d(d + kVHalf, &vmap, h * kHeadDim + 128, vrows[k], bar,
+                                        stream);
+                        }
+                    }
+                } else if (ci == 1) {
+                    // every lane acquires the stage's release before the zeroing stores below
+                    if (!ctx.wait_warp(&sm.vfree[vs], ((tv / kVStages) & 1) ^ 1)) break;
+                    if (lane == 0) {
+                        int rows[kChunks];
+                        int nval = 0;
+#pragma unroll
+                        for (int c = 0; c < kChunks; ++c) {
+                            const int j0 = h0 + kChunk * c;
+                            rows[c] = j0 < end ? chunk_row(p, sm, b, start, j0, &clamped) : -1;
+                            nval += rows[c] >= 0;
+                        }
+                        const uint32_t bar = smem_u32(&sm.vtail);
+                        mbar_arrive_expect_tx(bar, nval * kChunk * kHeadDim);
+                        const uint32_t dst = smem_u32(vstage);
+#pragma unroll
+                        for (int c = 0; c < kChunks; ++c) {
+                            if (rows[c] < 0) continue;
+                            tma_load_2d(dst + c * 2048, &vmap, h * kHeadDim, rows[c], bar, stream);
+                            tma_load_2d(dst + c * 2048 + kVHalf, &vmap, h * kHeadDim + 128, rows[c],
+                                        bar, stream);
+                        }
+                    }
+                    tail_pending = true;
+                    if (!ctx.wait_warp(&sm.vtail, 0)) break;
+                    tail_pending = false;
+                    // keys nkeys..127 (page-tail slots or never-copied rows); a key's 128 bytes
+                    // per half are contiguous
+                    const int zero_chunks = (kVKeys - nkeys) * 8;  // 16-byte chunks per half
+                    for (int i = lane; i < 2 * zero_chunks; i += 32) {
+                        const int dh = i / zero_chunks, c = i % zero_chunks;
+                        *reinterpret_cast<uint4*>(vstage + dh * kVHalf + nkeys * 128 + c * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&sm.vfull[vs]));
+                } else {
+                    if (lane == 0) mbar_arrive(smem_u32(&sm.vfull[vs]));
+                }
+                if (lane == 0 && tv + 1 < nvst) own_rows(h0 + kVKeys, vfirst, vrows);
+                ++tv;
+                progressed = true;
+            }
+            if (progressed) {
+                idle = 0;
+                last = globaltimer_ns();
+            } else if ((++idle & 15) == 0) {
+                if (ctx.aborted()) break;
+                if (globaltimer_ns() - last > kWaitLimitNs) {
+                    if (lane == 0) {
+                        *reinterpret_cast<volatile int*>(&sm.abort) = 1;
+                        atomicOr(p.status, DFLASH_FLAG_KERNEL_TIMEOUT);
+                    }
+                    break;
+                }
+            }
+        }
+        if (lane == 0) {
             if (clamped) atomicOr(p.status, DFLASH_FLAG_PAGE_CLAMPED);
-            // no copy may still be writing shared memory when the CTA retires
-            for (int t = kdone - kKStages < 0 ? 0 : kdone - kKStages; t < kdone; ++t)
+            // no copy of this warp may still be writing shared memory when the CTA retires
+            for (int t = tk - kKStages < 0 ? 0 : tk - kKStages; t < tk; ++t)
                 mbar_wait(smem_u32(&sm.kfull[t % kKStages]), (t / kKStages) & 1, &sm.abort,
                           kWaitLimitNs);
+            for (int u = tv - kVStages < 0 ? 0 : tv - kVStages; u < tv; ++u) {
+                if (end - (start + u * kVKeys) < kVKeys) {
+                    if (tail_pending) mbar_wait(smem_u32(&sm.vtail), 0, &sm.abort, kWaitLimitNs);
+                } else {
+                    mbar_wait(smem_u32(&sm.vfull[u % kVStages]), (u / kVStages) & 1, &sm.abort,
+                              kWaitLimitNs);
+                }
+            }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
@@ -530,6 +656,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         if (lane == 0) mma_commit(smem_u32(&sm.odone));  // tracks every MMA issued above
     } else if (warp == 2) {
         // ------------------------------------------- V copies (TMA): 32-key stages, whole warp
+        const uint64_t stream = l2_evict_first_policy();  // every V page is read once
         bool clamped = false;
         int vdone = 0;
         bool tail_pending = false;  // the ragged last stage's copies are issued but not awaited
@@ -558,8 +685,9 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < kVKeys / kChunk; ++c) {
                     if (rows[c] < 0) continue;
-                    tma_load_2d(dst + c * 2048, &vmap, h * kHeadDim, rows[c], bar);
-                    tma_load_2d(dst + c * 2048 + kVHalf, &vmap, h * kHeadDim + 128, rows[c], bar);
+                    tma_load_2d(dst + c * 2048, &vmap, h * kHeadDim, rows[c], bar, stream);
+                    tma_load_2d(dst + c * 2048 + kVHalf, &vmap, h * kHeadDim + 128, rows[c], bar,
+                                stream);
                 }
             }
             vdone = u + 1;
@@ -695,7 +823,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         for (int t = 0; alive && t < ntiles; ++t) {
             const int tile0 = start + t * kTile;
             const int j = tile0 + st;
-            if (!ctx.wait_warp(&sm.sfull, t & 1)) {
+            if (!ctx.wait_lane0(&sm.sfull, t & 1)) {
                 alive = false;
                 break;
             }

@@ -95,6 +95,24 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tensor_map
         : "memory");
 }
 
+// L2 cache policy for data read exactly once: its lines are evicted first, so a stream of pages
+// larger than L2 does not push the kernel's code, tables and split state out of it.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+    return policy;
+}
+
+// tma_load_2d with an L2 cache policy for the copied lines.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tensor_map, int x, int y,
+                                            uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tensor_map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void named_barrier(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -124,13 +142,13 @@ __device__ __forceinline__ uint64_t pk2(float lo, float hi) {
     return r;
 }
 __device__ __forceinline__ float lo2(uint64_t x) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+    float lo;
+    asm("{\n\t.reg .f32 unused;\n\tmov.b64 {%0, unused}, %1;\n\t}" : "=f"(lo) : "l"(x));
     return lo;
 }
 __device__ __forceinline__ float hi2(uint64_t x) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+    float hi;
+    asm("{\n\t.reg .f32 unused;\n\tmov.b64 {unused, %0}, %1;\n\t}" : "=f"(hi) : "l"(x));
     return hi;
 }
 __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
