@@ -73,10 +73,15 @@ constexpr int kVStages = 3;
 constexpr int kSlices = kTile / 32;             // 32-key P slices of a tile (one per lane quadrant)
 constexpr int kSlicesPerStage = kVKeys / 32;    // slices a V stage's MMA step consumes
 
-constexpr uint32_t kKStage = kTile * kHeadDim;   // 32768: two 128-byte column blocks of 128 keys
-constexpr uint32_t kVStage = kVKeys * kHeadDim;  // 32768: two 128-byte column blocks of 128 keys
-constexpr uint32_t kKHalf = kKStage / 2;
-constexpr uint32_t kVHalf = kVStage / 2;
+// K and V stages hold their 16-key chunks (one 4 KB page box each) back to back; inside a chunk,
+// [8-key group i][head-dim half h][key e][128 bytes] with the 128-byte swizzle, so the 8-key group
+// g of the stage (keys 8g..8g+7) of half h starts at g * kGroupStride + h * kHalfOffset: one
+// uniform group stride for the MMA descriptors, keys in their natural order.
+constexpr uint32_t kKStage = kTile * kHeadDim;   // 32768
+constexpr uint32_t kVStage = kVKeys * kHeadDim;  // 32768
+constexpr uint32_t kChunkBytes = kChunk * kHeadDim;  // 4096
+constexpr uint32_t kGroupStride = 2048;              // 8 keys x both halves
+constexpr uint32_t kHalfOffset = 1024;               // 8 keys x 128 bytes
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
 constexpr int kRowCache = 128;  // 16-key chunks of a split whose source row is looked up up front
 constexpr float kPShift = 4.f;         // s: probabilities are scaled by 2^s before the split
@@ -469,9 +474,8 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < kOwn; ++k) {
                         if (krows[k] < 0) continue;
-                        const uint32_t d = dst + (kfirst + 3 * k) * 2048;
-                        tma_load_2d(d, &kmap, h * kHeadDim, krows[k], bar, stream);
-                        tma_load_2d(d + kKHalf, &kmap, h * kHeadDim + 128, krows[k], bar, stream);
+                        tma_load_4d(dst + (kfirst + 3 * k) * kChunkBytes, &kmap, 0, 0, 2 * h,
+                                    krows[k] / 8, bar, stream);
                     }
                     if (tk + 1 < ntiles) own_rows(start + (tk + 1) * kTile, kfirst, krows);
                 }
@@ -494,10 +498,8 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
 #pragma unroll
                         for (int k = 0; k < kOwn; ++k) {
                             if (vrows[k] < 0) continue;
-                            const uint32_t d = dst + (vfirst + 3 * k) * 2048;
-                            tma_load_2d(d, &vmap, h * kHeadDim, vrows[k], bar, stream);
-                            tma_load_2d(d + kVHalf, &vmap, h * kHeadDim + 128, vrows[k], bar,
-                                        stream);
+                            tma_load_4d(dst + (vfirst + 3 * k) * kChunkBytes, &vmap, 0, 0, 2 * h,
+                                        vrows[k] / 8, bar, stream);
                         }
                     }
                 } else if (ci == 1) {
@@ -518,20 +520,20 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
 #pragma unroll
                         for (int c = 0; c < kChunks; ++c) {
                             if (rows[c] < 0) continue;
-                            tma_load_2d(dst + c * 2048, &vmap, h * kHeadDim, rows[c], bar, stream);
-                            tma_load_2d(dst + c * 2048 + kVHalf, &vmap, h * kHeadDim + 128, rows[c],
-                                        bar, stream);
+                            tma_load_4d(dst + c * kChunkBytes, &vmap, 0, 0, 2 * h, rows[c] / 8, bar,
+                                        stream);
                         }
                     }
                     tail_pending = true;
                     if (!ctx.wait_warp(&sm.vtail, 0)) break;
                     tail_pending = false;
                     // keys nkeys..127 (page-tail slots or never-copied rows); a key's 128 bytes
-                    // per half are contiguous
-                    const int zero_chunks = (kVKeys - nkeys) * 8;  // 16-byte chunks per half
-                    for (int i = lane; i < 2 * zero_chunks; i += 32) {
-                        const int dh = i / zero_chunks, c = i % zero_chunks;
-                        *reinterpret_cast<uint4*>(vstage + dh * kVHalf + nkeys * 128 + c * 16) =
+                    // per half are contiguous (the swizzle permutes 16-byte units inside them)
+                    const int zero_units = (kVKeys - nkeys) * 16;  // 16-byte units, both halves
+                    for (int i = lane; i < zero_units; i += 32) {
+                        const int key = nkeys + i / 16, dh = (i / 8) & 1, u = i & 7;
+                        *reinterpret_cast<uint4*>(vstage + (key / 8) * kGroupStride +
+                                                  dh * kHalfOffset + (key % 8) * 128 + u * 16) =
                             make_uint4(0, 0, 0, 0);
                     }
                     fence_async_smem();
@@ -599,8 +601,8 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                     const uint32_t kb = smem_u32(smem + C::kOffK + s * kKStage);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t ad = smem_desc(kb + (kk >> 2) * kKHalf + (kk & 3) * 32, 16,
-                                                      1024, kSwizzle128B);
+                        const uint64_t ad = smem_desc(kb + (kk >> 2) * kHalfOffset + (kk & 3) * 32,
+                                                      16, kGroupStride, kSwizzle128B);
                         const uint64_t bd = smem_desc(
                             q_base + (kk >> 2) * (SN * 128) + (kk & 3) * 32, 16, 1024, kSwizzle128B);
                         mma_f8_ss(tmem + C::kColS, ad, bd, idesc_qk, kk > 0);
@@ -629,8 +631,10 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                                 smem_desc(pbase + kk * 512, 128, 2048, kSwizzleNone);
 #pragma unroll
                             for (int dh = 0; dh < 2; ++dh) {
-                                const uint64_t ad = smem_desc(vb + dh * kVHalf + kq * 4096, 4096,
-                                                              1024, kSwizzle128B);
+                                // 32 keys = four 8-key groups from group 4 kq on
+                                const uint64_t ad =
+                                    smem_desc(vb + dh * kHalfOffset + kq * 4 * kGroupStride,
+                                              kVStage, kGroupStride, kSwizzle128B);
                                 mma_f8_ss(tmem + C::kColO + dh * SN, ad, bd, idesc_pv,
                                           (t | kk) != 0);
                             }
@@ -654,73 +658,6 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             }
         }
         if (lane == 0) mma_commit(smem_u32(&sm.odone));  // tracks every MMA issued above
-    } else if (warp == 2) {
-        // ------------------------------------------- V copies (TMA): 32-key stages, whole warp
-        const uint64_t stream = l2_evict_first_policy();  // every V page is read once
-        bool clamped = false;
-        int vdone = 0;
-        bool tail_pending = false;  // the ragged last stage's copies are issued but not awaited
-        for (int u = 0; u < nvst; ++u) {
-            const int vs = u % kVStages;
-            const int h0 = start + u * kVKeys;
-            const int nkeys = min(kVKeys, end - h0);
-            const bool tail = nkeys < kVKeys;
-            if (!ctx.wait_warp(&sm.vfree[vs], ((u / kVStages) & 1) ^ 1)) break;
-            uint8_t* vstage = smem + C::kOffV + vs * kVStage;
-            const uint32_t bar = smem_u32(tail ? &sm.vtail : &sm.vfull[vs]);
-            if (lane == 0) {
-                int rows[kVKeys / kChunk];
-                int nval = 0;
-#pragma unroll
-                for (int c = 0; c < kVKeys / kChunk; ++c) {
-                    const int j0 = h0 + kChunk * c;
-                    rows[c] = -1;
-                    if (j0 < end) {
-                        rows[c] = chunk_row(p, sm, b, start, j0, &clamped);
-                        ++nval;
-                    }
-                }
-                mbar_arrive_expect_tx(bar, nval * kChunk * kHeadDim);
-                const uint32_t dst = smem_u32(vstage);
-#pragma unroll
-                for (int c = 0; c < kVKeys / kChunk; ++c) {
-                    if (rows[c] < 0) continue;
-                    tma_load_2d(dst + c * 2048, &vmap, h * kHeadDim, rows[c], bar, stream);
-                    tma_load_2d(dst + c * 2048 + kVHalf, &vmap, h * kHeadDim + 128, rows[c], bar,
-                                stream);
-                }
-            }
-            vdone = u + 1;
-            if (tail) {
-                // keys nkeys..63 of this stage (page-tail slots or never-copied rows) are zeroed
-                // once the copies have landed; a key's 128 bytes per half are contiguous
-                tail_pending = true;
-                if (!ctx.wait_warp(&sm.vtail, 0)) break;
-                tail_pending = false;
-                const int zero_chunks = (kVKeys - nkeys) * 8;  // 16-byte chunks per half
-                for (int i = lane; i < 2 * zero_chunks; i += 32) {
-                    const int dh = i / zero_chunks, c = i % zero_chunks;
-                    *reinterpret_cast<uint4*>(vstage + dh * kVHalf + nkeys * 128 + c * 16) =
-                        make_uint4(0, 0, 0, 0);
-                }
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sm.vfull[vs]));
-            }
-        }
-        if (lane == 0) {
-            if (clamped) atomicOr(p.status, DFLASH_FLAG_PAGE_CLAMPED);
-            // no copy may still be writing shared memory when the CTA retires
-            for (int u = vdone - kVStages < 0 ? 0 : vdone - kVStages; u < vdone; ++u) {
-                const bool is_tail = end - (start + u * kVKeys) < kVKeys;
-                if (is_tail) {
-                    if (tail_pending) mbar_wait(smem_u32(&sm.vtail), 0, &sm.abort, kWaitLimitNs);
-                } else {
-                    mbar_wait(smem_u32(&sm.vfull[u % kVStages]), (u / kVStages) & 1, &sm.abort,
-                              kWaitLimitNs);
-                }
-            }
-        }
     } else if (warp >= 4) {
         // ------------------------------------------------------------- softmax (RP/16 groups)
         const int sw = warp - 4;          // 0 .. kSoftWarps - 1
@@ -1114,19 +1051,23 @@ cudaError_t launch_tc_partial(const PartialParams& p, cudaStream_t stream) {
     if (rp > tc::kMaxRP) return cudaErrorInvalidValue;
     const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
-    // K and V pools viewed as [num_pages * page_size rows, Hkv * 256 bytes]; both copied in boxes
-    // of 16 rows x 128 bytes into the 128-byte swizzle the MMA operands use
+    // K and V pools (rows of Hkv * 256 bytes, num_pages * page_size of them) viewed as 4-D:
+    // (byte within a 128-byte head-dim half, row within an 8-row group, half index 2 h + half,
+    // 8-row group). A box (128, 8, 2, 2) is one 16-row chunk of one head, both halves, landing as
+    // [group][half][row][128 bytes] in the 128-byte swizzle the MMA operands use: one copy
+    // instruction per 4 KB page chunk. Rows of a chunk start at a multiple of 16 (pages are).
     CUtensorMap kmap, vmap;
-    const cuuint64_t dims[2] = {(cuuint64_t)p.num_kv_heads * kHeadDim,
-                                (cuuint64_t)p.num_pages * p.page_size};
-    const cuuint64_t strides[1] = {(cuuint64_t)p.num_kv_heads * kHeadDim};
-    const cuuint32_t box[2] = {128, tc::kChunk};
-    const cuuint32_t estride[2] = {1, 1};
-    CUresult r1 = encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.k_pool),
+    const cuuint64_t row = (cuuint64_t)p.num_kv_heads * kHeadDim;
+    const cuuint64_t dims[4] = {128, 8, 2 * (cuuint64_t)p.num_kv_heads,
+                                (cuuint64_t)p.num_pages * p.page_size / 8};
+    const cuuint64_t strides[3] = {row, 128, 8 * row};
+    const cuuint32_t box[4] = {128, 8, 2, 2};
+    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    CUresult r1 = encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(p.k_pool),
                          dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    CUresult r2 = encode(&vmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.v_pool),
+    CUresult r2 = encode(&vmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(p.v_pool),
                          dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -113,6 +113,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tensor_map
         : "memory");
 }
 
+// 4-D tiled tensor copy global -> shared with an L2 cache policy; coordinates innermost first.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tensor_map, int c0, int c1,
+                                            int c2, int c3, uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tensor_map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar),
+        "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void named_barrier(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
