@@ -68,16 +68,20 @@ __device__ __forceinline__ int keys_per_split(int n, int num_splits, int tile_ke
     return (per + tile_keys - 1) / tile_keys * tile_keys;
 }
 
-// Physical page of logical page lp of sequence b, clamped into the pool.
-__device__ __forceinline__ int physical_page(const int32_t* block_table, int b,
-                                             int max_pages_per_seq, int lp, int num_pages,
-                                             bool* clamped) {
-    int phys = block_table[(int64_t)b * max_pages_per_seq + lp];
+// A block-table entry clamped into the pool of num_pages pages.
+__device__ __forceinline__ int clamp_page(int phys, int num_pages, bool* clamped) {
     if (phys < 0 || phys >= num_pages) {
         *clamped = true;
         phys = phys < 0 ? 0 : num_pages - 1;
     }
     return phys;
+}
+
+// Physical page of logical page lp of sequence b, clamped into the pool.
+__device__ __forceinline__ int physical_page(const int32_t* block_table, int b,
+                                             int max_pages_per_seq, int lp, int num_pages,
+                                             bool* clamped) {
+    return clamp_page(block_table[(int64_t)b * max_pages_per_seq + lp], num_pages, clamped);
 }
 
 }  // namespace dflash

@@ -353,6 +353,16 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int R = p.rows, G = p.group, P = p.page_size;
 
+    // The split's key range follows from the context length, one load away. The range that a
+    // context of max_context keys gives is known now, and it is the actual range whenever the
+    // split size comes out the same (split sizes are whole tiles, so any context close to
+    // max_context): thread c looks up chunk c of that range while the length is in flight, and
+    // the row cache below takes it if the sizes agree.
+    const int per_max = keys_per_split(p.max_context, p.num_splits, p.tile_keys, p.min_split_keys);
+    int page_max = 0;
+    if (tid < kRowCache && split * per_max + tid * kChunk < p.max_context)
+        page_max = p.block_table[(int64_t)b * p.max_pages_per_seq +
+                                 (split * per_max + tid * kChunk) / P];
     int cflags;
     const int n = clamped_context(p.context_lens, b, p.max_context, &cflags);
     if (split == 0 && h == 0 && tid == 0) {
@@ -377,6 +387,8 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     // ---- set-up: barriers and tensor memory (Q terms are staged by the softmax warps while the
     // first copies are already in flight) ------------------------------------------------------
     if (tid == 0) {
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
         for (int i = 0; i < kKStages; ++i) {
             mbar_init(smem_u32(&sm.kfull[i]), 3);  // one arrival per copying warp
             mbar_init(smem_u32(&sm.kempty[i]), 1);
@@ -405,8 +417,10 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         const int nchunks = min((end - start + kChunk - 1) / kChunk, kRowCache);
         for (int c = tid; c < nchunks; c += C::kThreads) {
             const int j0 = start + c * kChunk;
-            const int phys = physical_page(p.block_table, b, p.max_pages_per_seq, j0 / P,
-                                           p.num_pages, &clamped);
+            const int phys = (per == per_max && c == tid)
+                                 ? clamp_page(page_max, p.num_pages, &clamped)
+                                 : physical_page(p.block_table, b, p.max_pages_per_seq, j0 / P,
+                                                 p.num_pages, &clamped);
             sm.rows[c] = phys * P + (j0 % P);
         }
         if (clamped) atomicOr(p.status, DFLASH_FLAG_PAGE_CLAMPED);

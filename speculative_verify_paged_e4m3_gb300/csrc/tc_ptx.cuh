@@ -95,6 +95,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tensor_map
         : "memory");
 }
 
+// Fetch a TMA descriptor (a kernel parameter) ahead of its first use.
+__device__ __forceinline__ void prefetch_tensormap(const void* tensor_map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tensor_map))
+                 : "memory");
+}
+
 // L2 cache policy for data read exactly once: its lines are evicted first, so a stream of pages
 // larger than L2 does not push the kernel's code, tables and split state out of it.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
