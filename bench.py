@@ -39,7 +39,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="c3", help="c0|c1|c2|c3|c4:<q_len>:<context>")
+    ap.add_argument("--config", default="c3",
+                    help="c0|c1|c2|c3|c4:<q_len>:<context>|c5|c6:<batch>:<context>")
     ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tcgen05")
     ap.add_argument("--splits", type=int, default=0, help="force the split count (0: planner)")
     ap.add_argument("--layers", type=int, default=0,
@@ -56,7 +57,11 @@ def workload(name):
     if name.startswith("c4"):
         _, q, n = name.split(":")
         return W.config4(int(q), int(n))
-    return {"c0": W.config0, "c1": W.config1, "c2": W.config2, "c3": W.config3}[name]()
+    if name.startswith("c6"):
+        _, bsz, n = name.split(":")
+        return W.config6(int(bsz), int(n))
+    return {"c0": W.config0, "c1": W.config1, "c2": W.config2, "c3": W.config3,
+            "c5": W.config5}[name]()
 
 
 def measured_peak():

@@ -9,7 +9,8 @@ module compiles it with gcc on first use and marshals NumPy arrays through ctype
 file's header for the definition it implements and the passages it follows.
 
 Pins (tests/test_oracle_pins.py): E4M3 decode against the OCP format's printed values and the
-library cast ``torch.float8_e4m3fn``; tiny cases against torch's float64 scaled-dot-product
+library cast ``torch.float8_e4m3fn``; E4M3 encode by round trip over every code, midpoints
+(ties to even), saturation and the library cast; the KV write on hand-placed tokens; tiny cases against torch's float64 scaled-dot-product
 attention (a library routine); uniform- and one-hot-softmax closed forms; block-table permutation
 and page-size invariance; split/merge agreement; the q_len = 1 reduction; planted mistakes.
 """
@@ -65,6 +66,13 @@ class Oracle:
         lib.oracle_merge_partials.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, _dp,
                                               _dp, _dp, _dp, _dp]
         lib.oracle_merge_partials.restype = None
+        lib.oracle_e4m3_encode_array.argtypes = [_dp, ctypes.c_int64, _u8p]
+        lib.oracle_e4m3_encode_array.restype = None
+        _fp = ctypes.POINTER(ctypes.c_float)
+        lib.oracle_kv_write.argtypes = [ctypes.c_int] * 8 + [_fp, _fp, _i32p, _i32p,
+                                                               ctypes.c_float, ctypes.c_float,
+                                                               _u8p, _u8p]
+        lib.oracle_kv_write.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         self.lib = lib
@@ -78,6 +86,40 @@ class Oracle:
         out = np.empty(codes.shape, dtype=np.float64)
         self.lib.oracle_e4m3_decode(_ptr(codes, _u8p), codes.size, _ptr(out, _dp))
         return out
+
+    def e4m3_encode(self, values) -> np.ndarray:
+        """E4M3FN codes of real values (nearest, ties to even, saturated to +-448)."""
+        v = np.ascontiguousarray(values, dtype=np.float64)
+        out = np.empty(v.shape, dtype=np.uint8)
+        self.lib.oracle_e4m3_encode_array(_ptr(v, _dp), v.size, _ptr(out, _u8p))
+        return out
+
+    def kv_write(self, k_new, v_new, block_table, context_lens, k_scale, v_scale, k_pool, v_pool,
+                 max_context):
+        """Write the drafted tokens' K/V rows into copies of the pools.
+
+        k_new, v_new: FP16 values [B, q_len, Hkv, D]; pools uint8 [num_pages, P, Hkv, D].
+        Returns (k_pool, v_pool, flags) with flags as oracle_kv_write returns them.
+        """
+        fp = ctypes.POINTER(ctypes.c_float)
+        k_new = np.ascontiguousarray(np.asarray(k_new).astype(np.float32))
+        v_new = np.ascontiguousarray(np.asarray(v_new).astype(np.float32))
+        k_pool = np.array(k_pool, dtype=np.uint8, copy=True, order="C")
+        v_pool = np.array(v_pool, dtype=np.uint8, copy=True, order="C")
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        B, q_len, Hkv, D = k_new.shape
+        num_pages, P, Hkv_p, D_p = k_pool.shape
+        if (Hkv_p, D_p) != (Hkv, D) or v_new.shape != k_new.shape or v_pool.shape != k_pool.shape:
+            raise ValueError("kv_write: shapes disagree")
+        if bt.ndim != 2 or bt.shape[0] != B or cl.shape != (B,):
+            raise ValueError("kv_write: block_table must be [B, max_pages] and context_lens [B]")
+        flags = self.lib.oracle_kv_write(B, q_len, Hkv, D, P, bt.shape[1], num_pages,
+                                         int(max_context), k_new.ctypes.data_as(fp),
+                                         v_new.ctypes.data_as(fp), _ptr(bt, _i32p),
+                                         _ptr(cl, _i32p), float(k_scale), float(v_scale),
+                                         _ptr(k_pool, _u8p), _ptr(v_pool, _u8p))
+        return k_pool, v_pool, int(flags)
 
     @staticmethod
     def _common(q, k_pool, v_pool, block_table, context_lens, k_scale, v_scale):

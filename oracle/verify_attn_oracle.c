@@ -298,3 +298,91 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/*
+ * E4M3FN code of a real value v, from the format's definition: the finite code whose value is
+ * nearest to v, ties going to the code with the even mantissa (round to nearest even), magnitudes
+ * of 448 and above saturated to 448 (the saturating conversion: S.1111.111 is NaN, not a larger
+ * number), NaN to the NaN code 0x7F. The sign bit follows v, so -0 gives 0x80. A search over the
+ * 127 non-negative finite codes: slow and plainly the definition.
+ */
+uint8_t oracle_e4m3_encode(double v)
+{
+    if (isnan(v))
+        return 0x7F;
+    const int neg = signbit(v) ? 1 : 0;
+    const double a = fabs(v);
+    int best = 0x7E;
+    if (a < 448.0) {
+        double best_err = INFINITY;
+        for (int c = 0; c <= 0x7E; ++c) {
+            const double err = fabs(oracle_e4m3_value((uint8_t)c) - a);
+            /* a tie is between neighbours c - 1 and c: keep the even one */
+            if (err < best_err || (err == best_err && (c & 1) == 0)) {
+                best = c;
+                best_err = err;
+            }
+        }
+    }
+    return (uint8_t)(best | (neg << 7));
+}
+
+void oracle_e4m3_encode_array(const double* v, int64_t n, uint8_t* codes)
+{
+    for (int64_t t = 0; t < n; ++t)
+        codes[t] = oracle_e4m3_encode(v[t]);
+}
+
+/*
+ * The step before verification: the q_len drafted tokens' K and V rows written into the paged
+ * pools as E4M3 codes. The pages imply it ("[Perf] Add opt-in DFlash2 schedules and numerical
+ * audits", Test Plan: E4M3 target KV) without describing it; this is the plain reading, the
+ * inverse of the decode above:
+ *   n    = context_lens[b] clamped to [0, max_context]       (as the attention clamps it)
+ *   pos  = n - q_len + i             (drafted token i sits where the causal rule places it)
+ *   page = block_table[b][pos / P],  slot = pos % P
+ *   code = oracle_e4m3_encode(x / scale), the quotient taken in FP32 (single precision, one
+ *          correctly rounded division: the precision the kernel decides the byte in)
+ * A token with pos < 0, or whose page entry lies outside [0, num_pages), is not written.
+ * k_new, v_new: [B, q_len, Hkv, D] holding exact FP16 values. Returns a bit set: 1 = a token had
+ * pos < 0, 2 = a page entry was out of range, 4 = context_lens[b] exceeded max_context.
+ */
+int oracle_kv_write(int B, int q_len, int Hkv, int D, int P, int max_pages_per_seq, int num_pages,
+                    int max_context, const float* k_new, const float* v_new,
+                    const int32_t* block_table, const int32_t* context_lens, float k_scale,
+                    float v_scale, uint8_t* k_pool, uint8_t* v_pool)
+{
+    int flags = 0;
+    for (int b = 0; b < B; ++b) {
+        int n = context_lens[b];
+        if (n > max_context) {
+            n = max_context;
+            flags |= 4;
+        }
+        if (n < 0)
+            n = 0;
+        for (int i = 0; i < q_len; ++i) {
+            const int pos = n - q_len + i;
+            if (pos < 0) {
+                flags |= 1;
+                continue;
+            }
+            const int page = block_table[(int64_t)b * max_pages_per_seq + pos / P];
+            if (page < 0 || page >= num_pages) {
+                flags |= 2;
+                continue;
+            }
+            for (int h = 0; h < Hkv; ++h) {
+                const int64_t src = (((int64_t)b * q_len + i) * Hkv + h) * D;
+                const int64_t dst = (((int64_t)page * P + pos % P) * Hkv + h) * D;
+                for (int d = 0; d < D; ++d) {
+                    const float kq = k_new[src + d] / k_scale;
+                    const float vq = v_new[src + d] / v_scale;
+                    k_pool[dst + d] = oracle_e4m3_encode((double)kq);
+                    v_pool[dst + d] = oracle_e4m3_encode((double)vq);
+                }
+            }
+        }
+    }
+    return flags;
+}

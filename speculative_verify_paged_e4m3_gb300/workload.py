@@ -9,7 +9,8 @@ allocations), and the capacity boundary of "[Perf] Reduce DFlash2 long-context v
 decay", Purpose (service capacity 262144; boundary window 261888 input tokens).
 
 Recipe, per layer (seed = seed_base + 10 * layer + tensor id, seed_base = 1000 * config for
-configs 0-3 and 40000 + 1000 * q_len + 200 * context index for the tail sweep; tensor ids: 0 Q,
+configs 0-3 and 5, 40000 + 1000 * q_len + 200 * context index for the tail sweep and
+60000 + 1000 * batch for the batched whole-model config; tensor ids: 0 Q,
 1 K, 2 V, 3 block-table permutation, 4 boost mask, 5 fill of unused pool bytes):
   * Q ~ N(0, 1) in FP32, rounded to FP16.
   * K, V ~ N(0, 1) in FP32 over the N logical tokens; optionally a seeded fraction of K tokens is
@@ -171,6 +172,22 @@ def config4(q_len: int, context: int) -> Workload:
     """Tail-shape sweep point: q_len in 1..8, N in {4096, 65536, 262144}, 16 layers, page 16."""
     return Workload(f"c4_q{q_len}_ctx{context}_p16", layers=16, context=(context,), q_len=q_len,
                     seed_base=40000 + 1000 * q_len + 200 * _ctx_index(context))
+
+
+def config5() -> Workload:
+    """Whole-model head count on one GPU (Hq 24, Hkv 4: the four-way tensor-parallel shard of
+    q8 / Hq6 / Hkv1 un-sharded), N=261888, page 16, 16 layers."""
+    return Workload("c5_q8_hq24_hkv4_ctx261888_p16", layers=16, context=(261888,),
+                    num_q_heads=24, num_kv_heads=4, seed_base=5000)
+
+
+def config6(batch: int, context: int) -> Workload:
+    """A batch of `batch` sequences with whole-model heads (Hq 24, Hkv 4), 16 layers, page 16;
+    ragged lengths from `context` down to about half of it in equal steps (multiples of 16)."""
+    step = context // (2 * batch) // 16 * 16
+    lens = tuple(context - i * step for i in range(batch))
+    return Workload(f"c6_b{batch}_q8_hq24_hkv4_ctx{context}_p16", layers=16, context=lens,
+                    num_q_heads=24, num_kv_heads=4, seed_base=60000 + 1000 * batch)
 
 
 TAIL_QLENS = tuple(range(1, 9))

@@ -301,6 +301,152 @@ def pin_q1_reduction(orc):
         assert np.array_equal(o1[:, 0], out[:, i]) and np.array_equal(l1[:, 0], lse[:, i]), i
 
 
+def _spec_points():
+    """(code, value) pairs printed in the OCP table (tests/golden/e4m3_spec_points.txt)."""
+    pts = []
+    with open(os.path.join(GOLDEN, "e4m3_spec_points.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                c, v = line.split()
+                pts.append((int(c, 16), float(v)))
+    return pts
+
+
+def pin_e4m3_encode_spec_points(orc):
+    """Encode of the OCP table's printed finite values gives their codes (signed zero kept)."""
+    pts = [(c, v) for c, v in _spec_points() if not math.isnan(v)]
+    got = orc.e4m3_encode(np.array([v for _, v in pts]))
+    for (c, v), g in zip(pts, got):
+        assert g == c, f"value {v}: expected {c:#04x}, got {g:#04x}"
+
+
+def pin_e4m3_encode_midpoints_ties_to_even(orc):
+    """Halfway between two neighbouring finite codes (values from torch's float8 decode) the
+    even code wins; a hair either side, the nearer one."""
+    codes = np.arange(0x7F, dtype=np.uint8)  # 0x00 .. 0x7E, ascending values
+    vals = torch_decode(codes).numpy()
+    lo, hi = vals[:-1], vals[1:]
+    mid = (lo + hi) / 2  # exact in float64
+    got = orc.e4m3_encode(mid)
+    even = np.where(codes[:-1] % 2 == 0, codes[:-1], codes[1:])
+    assert np.array_equal(got, even), np.nonzero(got != even)
+    gap = hi - lo
+    assert np.array_equal(orc.e4m3_encode(mid - gap * 1e-6), codes[:-1])
+    assert np.array_equal(orc.e4m3_encode(mid + gap * 1e-6), codes[1:])
+    assert np.array_equal(orc.e4m3_encode(-mid), even | 0x80)
+
+
+def pin_e4m3_encode_vs_torch_cast(orc):
+    """Random FP32 values across the normal and subnormal range (|v| < 464, where the library
+    cast needs no saturation) against torch's float8_e4m3fn cast."""
+    rng = np.random.default_rng(7)
+    mag = np.exp2(rng.uniform(-12, np.log2(460), size=20000)).astype(np.float32)
+    v = (mag * rng.choice([-1, 1], size=mag.size)).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = orc.e4m3_encode(v.astype(np.float64))
+    assert np.array_equal(got, ref), np.nonzero(got != ref)
+
+
+def pin_e4m3_encode_saturation_nan_zero(orc):
+    """Largest finite magnitude 448 (code S.1111.110) for everything at or beyond it, NaN to the
+    NaN code, zeros keep their sign."""
+    big = np.array([448.0, 449.0, 463.99, 464.0, 480.0, 1e30, np.inf])
+    assert np.all(orc.e4m3_encode(big) == 0x7E)
+    assert np.all(orc.e4m3_encode(-big) == 0xFE)
+    assert orc.e4m3_encode(np.array([np.nan]))[0] & 0x7F == 0x7F
+    assert list(orc.e4m3_encode(np.array([0.0, -0.0, 2.0 ** -11, -2.0 ** -11]))) == [
+        0x00, 0x80, 0x00, 0x80]
+
+
+def _kv_case():
+    """Two sequences, three drafted tokens, two KV heads, D 8, page 4; pools filled with 0x55."""
+    pts = dict((v, c) for c, v in _spec_points() if not math.isnan(v))
+    vals = [1.0, 2.0, 0.5, -1.0, 448.0, 3.0, 256.0, 0.015625]
+    scale, v_scale = 0.5, 0.25
+    k_new = np.empty((2, 3, 2, 8), dtype=np.float16)
+    v_new = np.empty_like(k_new)
+    for b in range(2):
+        for i in range(3):
+            for h in range(2):
+                rot = (b * 5 + i * 3 + h) % 8
+                k_new[b, i, h] = [vals[(d + rot) % 8] * scale for d in range(8)]
+                v_new[b, i, h] = [-vals[(d + rot + 1) % 8] * v_scale for d in range(8)]
+    code = lambda x: pts[abs(x)] | (0x80 if x < 0 else 0)
+    pool = np.full((5, 4, 2, 8), 0x55, dtype=np.uint8)
+    return k_new, v_new, scale, v_scale, pool, code
+
+
+def pin_kv_write_hand_placed(orc):
+    """Drafted token i of a length-n sequence lands at position n - q_len + i (page via the block
+    table, slot = position mod page size); nothing else in the pools changes; a token before the
+    start is skipped and flagged."""
+    k_new, v_new, scale, v_scale, pool, code = _kv_case()
+    bt = np.array([[3, 0, -1], [4, -1, -1]], dtype=np.int32)
+    ctx = np.array([6, 2], dtype=np.int32)
+    kp, vp, flags = orc.kv_write(k_new, v_new, bt, ctx, scale, v_scale, pool, pool, 12)
+    ek, ev = pool.copy(), pool.copy()
+    # sequence 0: positions 3, 4, 5 -> (page 3, slot 3), (page 0, slot 0), (page 0, slot 1)
+    # sequence 1: positions -1 (skipped), 0, 1 -> (page 4, slot 0), (page 4, slot 1)
+    for b, i, page, slot in [(0, 0, 3, 3), (0, 1, 0, 0), (0, 2, 0, 1), (1, 1, 4, 0), (1, 2, 4, 1)]:
+        for h in range(2):
+            ek[page, slot, h] = [code(float(x) / scale) for x in k_new[b, i, h]]
+            ev[page, slot, h] = [code(float(x) / v_scale) for x in v_new[b, i, h]]
+    assert flags == 1, flags
+    assert np.array_equal(kp, ek) and np.array_equal(vp, ev)
+
+
+def pin_kv_write_clamps(orc):
+    """An out-of-pool page entry skips its token (flag 2); a length beyond max_context is clamped
+    to it (flag 4), so the tokens go to max_context - q_len + i."""
+    k_new, v_new, scale, v_scale, pool, code = _kv_case()
+    bt = np.array([[3, 7, 1], [2, 0, -1]], dtype=np.int32)
+    ctx = np.array([6, 9], dtype=np.int32)
+    kp, vp, flags = orc.kv_write(k_new, v_new, bt, ctx, scale, v_scale, pool, pool, 8)
+    ek = pool.copy()
+    # sequence 0: positions 3 (page 3, slot 3), 4 and 5 (page entry 7: out of the pool, skipped)
+    # sequence 1: length 9 clamped to 8: positions 5, 6, 7 -> page 0, slots 1, 2, 3
+    for b, i, page, slot in [(0, 0, 3, 3), (1, 0, 0, 1), (1, 1, 0, 2), (1, 2, 0, 3)]:
+        for h in range(2):
+            ek[page, slot, h] = [code(float(x) / scale) for x in k_new[b, i, h]]
+    assert flags == 2 | 4, flags
+    assert np.array_equal(kp, ek)
+
+
+def pin_kv_write_fp32_quotient_decides(orc):
+    """The byte is decided on the FP32 quotient: where x / scale in FP32 lands exactly on a
+    midpoint between two codes while the exact quotient lies above it, the code is the even
+    neighbour of the midpoint, not the upper one (found by search over FP32 scales)."""
+    codes = np.arange(0x38, 0x40, dtype=np.uint8)  # 1.0 .. 1.875
+    vals = torch_decode(codes).numpy()
+    found = None
+    # pairs whose lower code is even: there the FP32 tie gives the lower code, the exact
+    # quotient the upper one
+    for lo, hi in zip(vals[0:-1:2], vals[1::2]):
+        m = (lo + hi) / 2
+        for x in (1.0, 1.5, 3.0, 0.75, 1.25):
+            s = np.float32(x / m)
+            for cand in (s, np.nextafter(s, np.float32(0)), np.nextafter(s, np.float32(10))):
+                q32 = np.float32(np.float32(x) / cand)
+                exact = x / float(cand)  # float64: far closer than the FP32 ulp here
+                if q32 == np.float32(m) and exact > m:
+                    found = (x, cand, lo, hi)
+                    break
+            if found:
+                break
+        if found:
+            break
+    assert found is not None, "no FP32 midpoint case found"
+    x, s, lo, hi = found
+    k_new = np.full((1, 1, 1, 8), x, dtype=np.float16)
+    pool = np.zeros((1, 4, 1, 8), dtype=np.uint8)
+    kp, _, flags = orc.kv_write(k_new, k_new, np.array([[0]], np.int32), np.array([1], np.int32),
+                                float(s), float(s), pool, pool, 4)
+    want = orc.e4m3_encode(np.array([lo]))[0]
+    assert want % 2 == 0
+    assert flags == 0 and np.all(kp[0, 0, 0] == want), (kp[0, 0, 0], want, found)
+
+
 PINS = [
     pin_e4m3_spec_points,
     pin_e4m3_all_codes_vs_torch,
@@ -312,4 +458,11 @@ PINS = [
     pin_split_merge_agreement,
     pin_split_merge_exact_integers,
     pin_q1_reduction,
+    pin_e4m3_encode_spec_points,
+    pin_e4m3_encode_midpoints_ties_to_even,
+    pin_e4m3_encode_vs_torch_cast,
+    pin_e4m3_encode_saturation_nan_zero,
+    pin_kv_write_hand_placed,
+    pin_kv_write_clamps,
+    pin_kv_write_fp32_quotient_decides,
 ]

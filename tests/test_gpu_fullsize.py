@@ -11,7 +11,7 @@ from speculative_verify_paged_e4m3_gb300 import workload as W
 
 pytestmark = pytest.mark.gpu
 
-CASES = [W.config1(), W.config2(), W.config3()] + [
+CASES = [W.config1(), W.config2(), W.config3(), W.config5(), W.config6(4, 65536)] + [
     W.config4(q, n) for n in W.TAIL_CONTEXTS for q in W.TAIL_QLENS]
 
 

@@ -70,6 +70,12 @@ def test_page_sizes(kernel, P, n):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
+def test_whole_model_heads_ragged_batch(kernel):
+    # Hq 24 / Hkv 4 (the four-way shard un-sharded): four KV-head units per sequence
+    check(small("b2_hkv4", [1300, 700], Hq=24, Hkv=4, seed=41), kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 def test_batch_ragged_two_kv_heads(kernel):
     check(small("b3_hkv2", [1500, 17, 640], Hq=12, Hkv=2, seed=3), kernel)
 

@@ -26,6 +26,17 @@ MUTANTS = {
     "lse_without_max": ("double l = mx + log(sum);", "double l = log(sum);"),
     "partials_max_sign": ("double w = exp(score(&p, e4m3, b, i, hq, j) - mx);",
                           "double w = exp(mx - score(&p, e4m3, b, i, hq, j));"),
+    "encode_ties_to_odd": ("(err == best_err && (c & 1) == 0)", "(err == best_err && (c & 1) == 1)"),
+    "encode_truncates": ("if (err < best_err || (err == best_err && (c & 1) == 0)) {",
+                         "if (oracle_e4m3_value((uint8_t)c) <= a) {"),
+    "encode_sign_dropped": ("return (uint8_t)(best | (neg << 7));", "return (uint8_t)best;"),
+    "kv_write_position_shift": ("const int pos = n - q_len + i;", "const int pos = n - q_len + i + 1;"),
+    "kv_write_slot_off_by_one": ("const int64_t dst = (((int64_t)page * P + pos % P) * Hkv + h) * D;",
+                                 "const int64_t dst = (((int64_t)page * P + (pos + 1) % P) * Hkv + h) * D;"),
+    "kv_write_wrong_scale": ("const float vq = v_new[src + d] / v_scale;",
+                             "const float vq = v_new[src + d] / k_scale;"),
+    "kv_write_double_quotient": ("k_pool[dst + d] = oracle_e4m3_encode((double)kq);",
+                                 "k_pool[dst + d] = oracle_e4m3_encode((double)k_new[src + d] / k_scale);"),
 }
 
 
