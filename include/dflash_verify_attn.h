@@ -182,6 +182,29 @@ int dflash_verify_attn_forward(const dflash_verify_attn_plan_t* plan, const void
                                size_t workspace_bytes, void* out, float* lse, void* cuda_stream);
 
 /*
+ * The step before verification: write the q_len drafted tokens' K and V rows (FP16) into the
+ * paged pools as E4M3FN codes (the E4M3 target KV of "[Perf] Add opt-in DFlash2 schedules and
+ * numerical audits", Test Plan; the pages do not describe the write itself).
+ *   k_new, v_new  fp16 [batch, q_len, Hkv, head_dim], 4-byte aligned (device)
+ *   k_pool, v_pool  E4M3 [num_pages, page_size, Hkv, head_dim] (device), written in place
+ *   block_table, context_lens, k_scale, v_scale  as for run (device)
+ * Token i of sequence b goes to position n - q_len + i, n = context_lens[b] clamped to
+ * [0, max_context] (the position the attention's causal rule gives it): slot position %
+ * page_size of page block_table[b][position / page_size]. Each element is stored as the E4M3FN
+ * code of x / scale (one correctly rounded FP32 division, then round to nearest even, magnitudes
+ * beyond 448 saturated to 448, NaN to a NaN code). A token whose position is negative
+ * (DFLASH_FLAG_CONTEXT_SHORT) or whose page entry lies outside [0, num_pages)
+ * (DFLASH_FLAG_PAGE_CLAMPED) is not written; a clamped context sets DFLASH_FLAG_CONTEXT_CLAMPED.
+ * The flags go to the status word of workspace (>= plan->workspace_bytes, 256-byte aligned, the
+ * one run uses). No allocation, no synchronisation; capture-safe.
+ */
+int dflash_verify_attn_kv_write(const dflash_verify_attn_plan_t* plan, const void* k_new,
+                                const void* v_new, const int32_t* block_table,
+                                const int32_t* context_lens, const float* k_scale,
+                                const float* v_scale, void* k_pool, void* v_pool,
+                                void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/*
  * Debug export of the kernels' E4M3 decode (the same device function the tensor-core kernel uses
  * for K and V): decoded[t] = exact value of codes[t] (NaN for S.1111.111), scaled[t] =
  * decoded[t] * *scale rounded once to FP32. n >= 0 elements; all pointers device memory;

@@ -38,6 +38,7 @@ EXPORTED = (
     "dflash_verify_attn_debug_dequant",
     "dflash_verify_attn_read_flags",
     "dflash_verify_attn_forward_static_scratch",
+    "dflash_verify_attn_kv_write",
     "dflash_verify_attn_status_string",
 )
 
@@ -93,6 +94,7 @@ def load_library() -> ctypes.CDLL:
             lib.dflash_verify_attn_combine.argtypes = [pp, vp, sz, vp, vp, vp, vp]
             lib.dflash_verify_attn_forward.argtypes = [pp] + [vp] * 8 + [sz, vp, vp, vp]
             lib.dflash_verify_attn_forward_static_scratch.argtypes = [pp] + [vp] * 10
+            lib.dflash_verify_attn_kv_write.argtypes = [pp] + [vp] * 9 + [sz, vp]
             lib.dflash_verify_attn_debug_dequant.argtypes = [vp, i64, vp, vp, vp, vp]
             lib.dflash_verify_attn_read_flags.argtypes = [vp, ctypes.POINTER(ctypes.c_int32),
                                                           ctypes.c_int, vp]
@@ -209,6 +211,19 @@ def dflash_verify_attn_forward_static_scratch(plan: Plan, q, k_pool, v_pool, blo
     return rc
 
 
+def dflash_verify_attn_kv_write(plan: Plan, k_new, v_new, block_table, context_lens, k_scale,
+                                v_scale, k_pool, v_pool, workspace, stream=None,
+                                check=True) -> int:
+    rc = load_library().dflash_verify_attn_kv_write(
+        ctypes.byref(plan), _ptr(k_new), _ptr(v_new), _ptr(block_table), _ptr(context_lens),
+        _ptr(k_scale), _ptr(v_scale), _ptr(k_pool), _ptr(v_pool), _ptr(workspace),
+        workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0,
+        _stream(stream))
+    if check:
+        _check("dflash_verify_attn_kv_write", rc)
+    return rc
+
+
 def dflash_verify_attn_debug_dequant(codes, scale, decoded, scaled=None, stream=None):
     _check("dflash_verify_attn_debug_dequant",
            load_library().dflash_verify_attn_debug_dequant(
@@ -269,3 +284,9 @@ class VerifyAttention:
         dflash_verify_attn_forward(self.plan, q, k_pool, v_pool, block_table, context_lens,
                                    k_scale, v_scale, self.workspace, out, lse, stream)
         return out, lse
+
+    def kv_write(self, k_new, v_new, block_table, context_lens, k_scale, v_scale, k_pool,
+                 v_pool, stream=None):
+        """Write the drafted tokens' K/V rows ([B, q_len, Hkv, D] FP16) into the pools."""
+        dflash_verify_attn_kv_write(self.plan, k_new, v_new, block_table, context_lens, k_scale,
+                                    v_scale, k_pool, v_pool, self.workspace, stream)

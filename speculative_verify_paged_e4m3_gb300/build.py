@@ -18,7 +18,8 @@ LIB_NAME = "libdflash_verify_attn.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["api.cu", "simt_partial.cu", "tc_partial.cu", "combine.cu", "static_scratch.cu"]
+SOURCES = ["api.cu", "simt_partial.cu", "tc_partial.cu", "combine.cu", "static_scratch.cu",
+           "kv_write.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
           "-I", INCLUDE, "-I", CSRC]

@@ -18,6 +18,11 @@ namespace dflash {
 cudaError_t launch_simt_partial(const PartialParams& p, cudaStream_t stream);
 cudaError_t launch_tc_partial(const PartialParams& p, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+cudaError_t launch_kv_write(const dflash_verify_attn_plan_t* plan, const void* k_new,
+                            const void* v_new, const int32_t* block_table,
+                            const int32_t* context_lens, const float* k_scale,
+                            const float* v_scale, void* k_pool, void* v_pool, int32_t* status,
+                            cudaStream_t stream);
 size_t simt_smem_bytes();
 size_t tc_smem_bytes(int rows);
 int tc_threads(int rows);
@@ -161,7 +166,9 @@ int dflash_verify_attn_plan(const dflash_verify_attn_problem* pr,
         const int64_t cap = ceil_div(pr->max_context, plan->min_split_keys);
         if (S > cap) S = cap;
     } else if (S == 0) {
-        S = ceil_div(sm_count, units);  // one wave of single-CTA-per-SM work
+        // one wave of single-CTA-per-SM work: units * S <= SMs (a CTA past the SM count would
+        // wait for a second wave and double the launch time)
+        S = units < sm_count ? sm_count / units : 1;
         const int64_t cap = ceil_div(pr->max_context, plan->min_split_keys);
         if (S > cap) S = cap;
     }
@@ -221,6 +228,30 @@ int dflash_verify_attn_run(const dflash_verify_attn_plan_t* plan, const void* q,
     else
         return DFLASH_ERR_INVALID_ARGUMENT;
     if (e != cudaSuccess) {
+        cudaGetLastError();
+        return DFLASH_ERR_CUDA;
+    }
+    return DFLASH_OK;
+}
+
+int dflash_verify_attn_kv_write(const dflash_verify_attn_plan_t* plan, const void* k_new,
+                                const void* v_new, const int32_t* block_table,
+                                const int32_t* context_lens, const float* k_scale,
+                                const float* v_scale, void* k_pool, void* v_pool,
+                                void* workspace, size_t workspace_bytes, void* cuda_stream) {
+    int rc = check_plan(plan);
+    if (rc != DFLASH_OK) return rc;
+    if (!k_new || !v_new || !block_table || !context_lens || !k_scale || !v_scale || !k_pool ||
+        !v_pool || !workspace)
+        return DFLASH_ERR_INVALID_ARGUMENT;
+    if (!aligned(k_new, 4) || !aligned(v_new, 4) || !aligned(k_pool, 2) || !aligned(v_pool, 2) ||
+        !aligned(workspace, 256) || !aligned(block_table, 4) || !aligned(context_lens, 4))
+        return DFLASH_ERR_INVALID_ARGUMENT;
+    if (workspace_bytes < plan->workspace_bytes) return DFLASH_ERR_WORKSPACE_TOO_SMALL;
+    if (plan->problem.batch * plan->problem.q_len == 0) return DFLASH_OK;
+    if (launch_kv_write(plan, k_new, v_new, block_table, context_lens, k_scale, v_scale, k_pool,
+                        v_pool, static_cast<int32_t*>(workspace),
+                        static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) {
         cudaGetLastError();
         return DFLASH_ERR_CUDA;
     }

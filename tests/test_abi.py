@@ -184,3 +184,38 @@ def test_fused_forward_rejects_bad_arguments_without_launching(B):
     rc = lib.dflash_verify_attn_forward(ctypes.byref(plan), *args,
                                         ctypes.c_size_t(plan.workspace_bytes - 1), fake, fake, None)
     assert rc == B.DFLASH_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_kv_write_rejects_bad_arguments_without_launching(B):
+    plan = B.dflash_verify_attn_plan(problem(B))
+    lib = B.load_library()
+    fake = 4096
+    ws = ctypes.c_size_t(plan.workspace_bytes)
+    rc = lib.dflash_verify_attn_kv_write(ctypes.byref(plan), None, None, None, None, None, None,
+                                         None, None, None, ctypes.c_size_t(0), None)
+    assert rc == B.DFLASH_ERR_INVALID_ARGUMENT
+    # k_new must allow FP16 pairs (4-byte aligned); no device memory is touched before this check
+    rc = lib.dflash_verify_attn_kv_write(ctypes.byref(plan), fake + 2, fake, fake, fake, fake,
+                                         fake, fake, fake, fake, ws, None)
+    assert rc == B.DFLASH_ERR_INVALID_ARGUMENT
+    rc = lib.dflash_verify_attn_kv_write(ctypes.byref(plan), fake, fake, fake, fake, fake, fake,
+                                         fake, fake, fake, ctypes.c_size_t(plan.workspace_bytes - 1),
+                                         None)
+    assert rc == B.DFLASH_ERR_WORKSPACE_TOO_SMALL
+    rc = lib.dflash_verify_attn_kv_write(ctypes.byref(B.Plan()), fake, fake, fake, fake, fake,
+                                         fake, fake, fake, fake, ws, None)
+    assert rc == B.DFLASH_ERR_INVALID_ARGUMENT
+
+
+def test_default_split_count_fills_one_wave(B):
+    """One CTA per SM: the default plan keeps batch x KV heads x splits within the SM count (a CTA
+    past it would run in a second wave), and uses as many splits as fit."""
+    for batch, hkv in [(1, 1), (3, 1), (1, 4), (4, 4), (5, 7), (200, 1)]:
+        plan = B.dflash_verify_attn_plan(problem(B, batch=batch, num_q_heads=6 * hkv,
+                                                 num_kv_heads=hkv))
+        units = batch * hkv
+        if units <= plan.sm_count:
+            assert units * plan.num_splits <= plan.sm_count
+            assert units * (plan.num_splits + 1) > plan.sm_count
+        else:
+            assert plan.num_splits == 1
