@@ -121,8 +121,8 @@ typedef struct {
     int32_t sm_count;         /* SMs of plan.problem.device */
     int32_t combine_fused;    /* 1: forward merges the splits inside the partial-kernel launch */
     size_t workspace_bytes;   /* caller allocates at least this many bytes */
-    size_t ws_state_offset;   /* float2 (m, l) [batch, Hkv, S, R]; m in log2 units */
-    size_t ws_acc_offset;     /* float numerator [batch, Hkv, S, R, head_dim], v_scale applied */
+    size_t ws_state_offset;   /* float2 (m, l) [slots, R]; m in log2 units (slots below) */
+    size_t ws_acc_offset;     /* float numerator [slots, R, head_dim], v_scale applied */
     dflash_verify_attn_problem problem;
 } dflash_verify_attn_plan_t;
 
@@ -137,9 +137,28 @@ int dflash_verify_attn_plan(const dflash_verify_attn_problem* problem,
                             dflash_verify_attn_plan_t* plan);
 
 /*
- * Split boundaries the kernels use for a sequence of context length n (host restatement of the
- * device rule): keys_per_split = roundup(max(ceil(n / S), min_split_keys), tile_keys), split s
- * covers [s * keys_per_split, min(n, (s + 1) * keys_per_split)), and the first
+ * Split slots (host restatement of the device rule). The workspace holds slots = batch * Hkv *
+ * num_splits split states, one per partial-kernel CTA. They are shared out among the
+ * (sequence, KV head) units u = b * Hkv + h in proportion to the context lengths counted in
+ * 128-key granules g_u = ceil(n_b / 128) (n_b = context_lens[b] clamped to [0, max_context]):
+ *   slot_start[u] = (non-empty units before u) + floor((slots - E) * (g of the units before u) / G)
+ * with E the non-empty units and G the granules of all units, so that every non-empty unit owns
+ * at least one slot and an empty unit none; with equal lengths every unit owns num_splits slots
+ * (the [batch, Hkv, num_splits, R] layout). Unit u splits its n_b keys into pieces of
+ * keys_per_split[u] = roundup(max(ceil(n_b / S_u), min_split_keys), tile_keys) keys, S_u =
+ * slot_start[u + 1] - slot_start[u]; its first active[u] = ceil(n_b / keys_per_split[u]) slots
+ * hold state (0 for an empty unit). context_lens: batch entries (host memory); slot_start:
+ * batch * Hkv + 1 entries; keys_per_split and active: batch * Hkv entries.
+ */
+int dflash_verify_attn_split_slots(const dflash_verify_attn_plan_t* plan,
+                                   const int32_t* context_lens, int32_t* slot_start,
+                                   int32_t* keys_per_split, int32_t* active);
+
+/*
+ * Split boundaries the kernels use when every sequence of the batch has context length n (then
+ * every unit owns num_splits slots, dflash_verify_attn_split_slots): keys_per_split =
+ * roundup(max(ceil(n / S), min_split_keys), tile_keys), split s covers
+ * [s * keys_per_split, min(n, (s + 1) * keys_per_split)), and the first
  * *active = ceil(n / keys_per_split) splits are non-empty (0 when n == 0). n is clamped to
  * [0, max_context] first. starts[] receives S + 1 entries (host memory); empty splits start and
  * end at n.

@@ -32,6 +32,7 @@ DFLASH_KERNEL_TCGEN05 = 2
 EXPORTED = (
     "dflash_verify_attn_plan",
     "dflash_verify_attn_split_bounds",
+    "dflash_verify_attn_split_slots",
     "dflash_verify_attn_run",
     "dflash_verify_attn_combine",
     "dflash_verify_attn_forward",
@@ -90,6 +91,8 @@ def load_library() -> ctypes.CDLL:
             lib.dflash_verify_attn_plan.argtypes = [ctypes.POINTER(Problem), pp]
             lib.dflash_verify_attn_split_bounds.argtypes = [
                 pp, i32, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
+            i32p = ctypes.POINTER(ctypes.c_int32)
+            lib.dflash_verify_attn_split_slots.argtypes = [pp, i32p, i32p, i32p, i32p]
             lib.dflash_verify_attn_run.argtypes = [pp] + [vp] * 8 + [sz, vp]
             lib.dflash_verify_attn_combine.argtypes = [pp, vp, sz, vp, vp, vp, vp]
             lib.dflash_verify_attn_forward.argtypes = [pp] + [vp] * 8 + [sz, vp, vp, vp]
@@ -162,6 +165,22 @@ def dflash_verify_attn_split_bounds(plan: Plan, n: int):
            load_library().dflash_verify_attn_split_bounds(ctypes.byref(plan), int(n), starts,
                                                           ctypes.byref(active)))
     return list(starts), active.value
+
+
+def dflash_verify_attn_split_slots(plan: Plan, context_lens):
+    """(slot_start [units + 1], keys_per_split [units], active [units]) for the given host-side
+    context lengths (units = batch * Hkv, unit u = b * Hkv + h)."""
+    lens = list(int(x) for x in context_lens)
+    units = plan.problem.batch * plan.problem.num_kv_heads
+    if len(lens) != plan.problem.batch:
+        raise ValueError("context_lens must have batch entries")
+    cl = (ctypes.c_int32 * len(lens))(*lens)
+    start = (ctypes.c_int32 * (units + 1))()
+    per = (ctypes.c_int32 * units)()
+    act = (ctypes.c_int32 * units)()
+    _check("dflash_verify_attn_split_slots",
+           load_library().dflash_verify_attn_split_slots(ctypes.byref(plan), cl, start, per, act))
+    return list(start), list(per), list(act)
 
 
 def dflash_verify_attn_run(plan: Plan, q, k_pool, v_pool, block_table, context_lens, k_scale,

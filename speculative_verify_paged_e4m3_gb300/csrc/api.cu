@@ -11,6 +11,8 @@
 
 #include <mutex>
 
+#include <vector>
+
 #include "common.cuh"
 #include "e4m3.cuh"
 
@@ -184,6 +186,56 @@ int dflash_verify_attn_plan(const dflash_verify_attn_problem* pr,
     plan->ws_acc_offset = kHeaderBytes + align_up(state_bytes, 256);
     plan->workspace_bytes = plan->ws_acc_offset + acc_bytes;
     plan->problem = *pr;
+    return DFLASH_OK;
+}
+
+int dflash_verify_attn_split_slots(const dflash_verify_attn_plan_t* plan,
+                                   const int32_t* context_lens, int32_t* slot_start,
+                                   int32_t* keys_per_split, int32_t* active) {
+    int rc = check_plan(plan);
+    if (rc != DFLASH_OK) return rc;
+    if (!context_lens || !slot_start || !keys_per_split || !active)
+        return DFLASH_ERR_INVALID_ARGUMENT;
+    const dflash_verify_attn_problem& pr = plan->problem;
+    const int B = pr.batch, Hkv = pr.num_kv_heads;
+    std::vector<int64_t> n(B), g(B);
+    int64_t G = 0, E = 0;
+    for (int b = 0; b < B; ++b) {
+        int64_t nb = context_lens[b];
+        nb = nb > pr.max_context ? pr.max_context : nb;
+        nb = nb < 0 ? 0 : nb;
+        n[b] = nb;
+        g[b] = (nb + 127) / 128;
+        G += g[b] * Hkv;
+        E += g[b] > 0 ? Hkv : 0;
+    }
+    const int64_t slots = (int64_t)B * Hkv * plan->num_splits;
+    int64_t g_before = 0, e_before = 0;
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < Hkv; ++h) {
+            const int u = b * Hkv + h;
+            slot_start[u] = G == 0 ? 0 : (int32_t)(e_before + (slots - E) * g_before / G);
+            g_before += g[b];
+            e_before += g[b] > 0 ? 1 : 0;
+        }
+    }
+    slot_start[B * Hkv] = G == 0 ? 0 : (int32_t)slots;
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < Hkv; ++h) {
+            const int u = b * Hkv + h;
+            const int64_t cnt = slot_start[u + 1] - slot_start[u];
+            if (n[b] == 0 || cnt == 0) {
+                keys_per_split[u] = 0;
+                active[u] = 0;
+                continue;
+            }
+            int64_t per = ceil_div(n[b], cnt);
+            if (per < plan->min_split_keys) per = plan->min_split_keys;
+            per = ceil_div(per, plan->tile_keys) * plan->tile_keys;
+            keys_per_split[u] = (int32_t)per;
+            active[u] = (int32_t)ceil_div(n[b], per);
+        }
+    }
     return DFLASH_OK;
 }
 

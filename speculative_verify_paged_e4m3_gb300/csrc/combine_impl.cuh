@@ -38,16 +38,16 @@ __device__ __forceinline__ void combine_sync(int bar_id) {
 // be in flight at once; the 16 lanes are then merged the same way through shared memory. The split
 // state is read through L2 (ld.global.cg), so that state written by other CTAs of the same launch
 // is seen.
-// n_raw: context_lens[b] when the caller has loaded it already, else -1.
+// The unit's splits sit in workspace slots [first, first + count) (common.cuh, locate_slots);
+// n is its context length (clamped).
 __device__ __forceinline__ void combine_item(const CombineParams& p, int r, int quarter, int b,
                                              int h, int tid, int bar_id, CombineScratch& sh,
-                                             int n_raw = -1) {
+                                             int first, int count, int n) {
     const int sl = tid / kCombineCols, col = tid % kCombineCols;
-    int n = n_raw >= 0 ? n_raw : p.context_lens[b];
-    n = n > p.max_context ? p.max_context : n;
-    const int per = keys_per_split(n, p.num_splits, p.tile_keys, p.min_split_keys);
+    n = count > 0 ? n : 0;
+    const int per = n > 0 ? keys_per_split(n, count, p.tile_keys, p.min_split_keys) : 1;
     const int active = n > 0 ? (n + per - 1) / per : 0;
-    const int64_t base = ((int64_t)b * p.num_kv_heads + h) * p.num_splits;
+    const int64_t base = first;
     const int R = p.rows;
     const float4* acc4 = reinterpret_cast<const float4*>(p.ws_acc);
 

@@ -84,4 +84,155 @@ __device__ __forceinline__ int physical_page(const int32_t* block_table, int b,
     return clamp_page(block_table[(int64_t)b * max_pages_per_seq + lp], num_pages, clamped);
 }
 
+// ---- split slots of a batch -------------------------------------------------------------------
+// The plan's batch * Hkv * S split slots (one CTA each) are shared out among the (sequence, KV
+// head) units in proportion to their context lengths counted in 128-key granules: unit
+// u = b * Hkv + h owns the contiguous slots [start(u), start(u + 1)) with
+//   start(u) = (non-empty units before u) + floor((C - E) * (granules of the units before u) / W)
+// (C slots, E non-empty units, W granules of all units), so that every non-empty unit owns at
+// least one slot, an empty unit none, and units of equal length own S slots each (the
+// [batch, Hkv, S] layout). dflash_verify_attn_split_slots does the same integer arithmetic on
+// the host.
+struct UnitSlots {
+    int b, h;    // the unit (b = -1: no unit owns the slot)
+    int first;   // its first slot
+    int count;   // its slot count (its split count)
+    int n;       // context length of sequence b, clamped to [0, max_context]
+    int flags;   // DFLASH_FLAG_CONTEXT_* of the whole batch
+};
+
+__device__ __forceinline__ int slot_granules(int n) { return (n + 127) >> 7; }
+
+// The clamped length of sequence b; sets the batch's context flags.
+__device__ __forceinline__ int slot_length(const int32_t* context_lens, int b, int max_context,
+                                           int q_len, int* flags) {
+    int n = context_lens[b];
+    if (n > max_context) {
+        n = max_context;
+        *flags |= DFLASH_FLAG_CONTEXT_CLAMPED;
+    }
+    n = n < 0 ? 0 : n;
+    if (n < q_len) *flags |= DFLASH_FLAG_CONTEXT_SHORT;
+    return n;
+}
+
+// Slots of a single sequence: its units are equal, S slots each.
+__device__ __forceinline__ UnitSlots locate_slots_single(const int32_t* context_lens, int Hkv,
+                                                         int S, int max_context, int q_len,
+                                                         int key, bool by_slot) {
+    UnitSlots r = {-1, 0, 0, 0, 0, 0};
+    int flags = 0;
+    const int n = slot_length(context_lens, 0, max_context, q_len, &flags);
+    const int u = by_slot ? key / S : key;
+    r.flags = flags;
+    if (n == 0 || u >= Hkv) return r;
+    r.b = 0;
+    r.h = u;
+    r.first = u * S;
+    r.count = S;
+    r.n = n;
+    return r;
+}
+
+// Slots of a batch of several sequences. Warp-cooperative: every lane of the warp calls it with
+// the same arguments and gets the same result. by_slot: the unit owning slot key; else the slots
+// of unit key.
+__device__ __forceinline__ UnitSlots locate_slots_batch_body(const int32_t* context_lens,
+                                                             int B, int Hkv, int S,
+                                                             int max_context, int q_len,
+                                                             int key, bool by_slot) {
+    const int lane = threadIdx.x & 31;
+    UnitSlots r = {-1, 0, 0, 0, 0, 0};
+    auto length = [&](int b, int* flags) {
+        return slot_length(context_lens, b, max_context, q_len, flags);
+    };
+    // totals over the batch (per sequence; every KV head of a sequence has its weight)
+    long long W = 0;
+    int E = 0, flags = 0;
+    for (int b0 = 0; b0 < B; b0 += 32) {
+        const int w = b0 + lane < B ? slot_granules(length(b0 + lane, &flags)) : 0;
+        W += w;
+        E += w > 0;
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        W += __shfl_xor_sync(0xffffffffu, W, o);
+        E += __shfl_xor_sync(0xffffffffu, E, o);
+        flags |= __shfl_xor_sync(0xffffffffu, flags, o);
+    }
+    r.flags = flags;
+    if (W == 0) return r;
+    W *= Hkv;
+    E *= Hkv;
+    const long long rest = (long long)B * Hkv * S - E;
+    long long w_carry = 0;
+    int e_carry = 0;
+    for (int b0 = 0; b0 < B; b0 += 32) {
+        const int b = b0 + lane;
+        int unused = 0;
+        const int n = b < B ? length(b, &unused) : 0;
+        const int w = slot_granules(n);
+        long long sw = w;  // inclusive scans over the chunk
+        int se = w > 0;
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long tw = __shfl_up_sync(0xffffffffu, sw, o);
+            const int te = __shfl_up_sync(0xffffffffu, se, o);
+            if (lane >= o) {
+                sw += tw;
+                se += te;
+            }
+        }
+        const long long w_before = w_carry + sw - w;  // granules of the sequences before b
+        const int e_before = e_carry + se - (w > 0);   // non-empty sequences before b
+        // slot h of sequence b starts at
+        auto start = [&](long long wb0, int eb0, int wb, int hh) {
+            return (long long)Hkv * eb0 + (wb > 0 ? hh : 0) +
+                   rest * ((long long)Hkv * wb0 + (long long)hh * wb) / W;
+        };
+        bool mine;
+        if (by_slot)
+            mine = b < B && w > 0 && key >= start(w_before, e_before, w, 0) &&
+                   key < start(w_before, e_before, w, Hkv);
+        else
+            mine = b == key / Hkv;
+        const unsigned m = __ballot_sync(0xffffffffu, mine);
+        if (m) {
+            const int src = __ffs(m) - 1;
+            const long long wb0 = __shfl_sync(0xffffffffu, w_before, src);
+            const int eb0 = __shfl_sync(0xffffffffu, e_before, src);
+            const int wb = __shfl_sync(0xffffffffu, w, src);
+            const int nb = __shfl_sync(0xffffffffu, n, src);
+            int hh = 0;
+            if (by_slot) {
+                while (hh + 1 < Hkv && start(wb0, eb0, wb, hh + 1) <= key) ++hh;
+            } else {
+                hh = key % Hkv;
+            }
+            r.b = b0 + src;
+            r.h = hh;
+            r.first = (int)start(wb0, eb0, wb, hh);
+            r.count = (int)(start(wb0, eb0, wb, hh + 1) - r.first);
+            r.n = nb;
+            return r;
+        }
+        w_carry += __shfl_sync(0xffffffffu, sw, 31);
+        e_carry += __shfl_sync(0xffffffffu, se, 31);
+    }
+    return r;
+}
+
+static __device__ __noinline__ UnitSlots locate_slots_batch(const int32_t* context_lens, int B,
+                                                            int Hkv, int S, int max_context,
+                                                            int q_len, int key, bool by_slot) {
+    return locate_slots_batch_body(context_lens, B, Hkv, S, max_context, q_len, key, by_slot);
+}
+
+// The slots of a unit or the unit of a slot (see above). Warp-cooperative. The several-sequence
+// search is called out of line: it runs once per CTA, and the kernels' hot code stays compact.
+__device__ __forceinline__ UnitSlots locate_slots(const int32_t* context_lens, int B, int Hkv,
+                                                  int S, int max_context, int q_len, int key,
+                                                  bool by_slot) {
+    if (B == 1) return locate_slots_single(context_lens, Hkv, S, max_context, q_len, key, by_slot);
+    return locate_slots_batch(context_lens, B, Hkv, S, max_context, q_len, key, by_slot);
+}
+
 }  // namespace dflash

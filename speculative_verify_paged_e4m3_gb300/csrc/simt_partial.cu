@@ -44,19 +44,20 @@ __global__ void __launch_bounds__(kSimtThreads, 1) simt_partial_kernel(PartialPa
     float* Ps = Vs + kSimtTile * kHeadDim;          // [kMaxRows][kPStride]
     float* alpha_s = Ps + kMaxRows * kPStride;      // [kMaxRows]
 
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = p.group, R = p.rows;
 
-    int cflags;
-    const int n = clamped_context(p.context_lens, b, p.max_context, &cflags);
-    if (split == 0 && h == 0 && tid == 0) {
-        if (n < p.q_len) cflags |= DFLASH_FLAG_CONTEXT_SHORT;
-        if (cflags) atomicOr(p.status, cflags);
-    }
-    const int per = keys_per_split(n, p.num_splits, p.tile_keys, p.min_split_keys);
+    // this CTA's workspace slot and the (sequence, KV head) unit owning it (slots are shared out
+    // by context length; common.cuh)
+    const int slot = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    const UnitSlots us = locate_slots(p.context_lens, p.batch, p.num_kv_heads, p.num_splits,
+                                      p.max_context, p.q_len, slot, true);
+    if (slot == 0 && tid == 0 && us.flags) atomicOr(p.status, us.flags);
+    const int b = us.b, h = us.h, split = slot - us.first, n = us.n;
+    if (b < 0) return;
+    const int per = keys_per_split(n, us.count, p.tile_keys, p.min_split_keys);
     const int start = split * per;
-    if (start >= n) return;  // idle split: the combine never reads it
+    if (start >= n) return;  // idle slot: the combine never reads it
     const int end = min(n, start + per);
 
     const float qscale = __ldg(p.k_scale) * 0.0625f * kLog2e;  // D = 256: D^-1/2 = 1/16
@@ -156,7 +157,7 @@ __global__ void __launch_bounds__(kSimtThreads, 1) simt_partial_kernel(PartialPa
     }
     if (page_clamped) atomicOr(p.status, DFLASH_FLAG_PAGE_CLAMPED);
 
-    const int64_t unit = ((int64_t)b * p.num_kv_heads + h) * p.num_splits + split;
+    const int64_t unit = slot;  // this split's workspace slot
 #pragma unroll
     for (int m = 0; m < kMaxRows / 8; ++m) {
         const int r = warp + 8 * m;

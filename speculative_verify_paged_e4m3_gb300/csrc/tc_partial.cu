@@ -305,11 +305,7 @@ __device__ __forceinline__ void fused_merge(const PartialParams& p, uint8_t* sme
     const int cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
     const int workers = gridDim.x * gridDim.y * gridDim.z * kHalves;
     const int items = p.batch * p.num_kv_heads * p.rows * kQuarters;
-    // the context length of this worker's first item is loaded while the barrier is pending
     const int first = cta * kHalves + half;
-    const int n_first =
-        (half < kHalves && first < items) ? p.context_lens[first / (kQuarters * p.rows) /
-                                                           p.num_kv_heads] : 0;
     __syncthreads();
     if (threadIdx.x == 0)
         *barrier_ok = grid_barrier(p.grid_bar, gridDim.x * gridDim.y * gridDim.z, p.status);
@@ -336,8 +332,10 @@ __device__ __forceinline__ void fused_merge(const PartialParams& p, uint8_t* sme
     for (int it = first; it < items; it += workers) {
         const int quarter = it % kQuarters, r = (it / kQuarters) % p.rows;
         const int unit = it / (kQuarters * p.rows);
+        const UnitSlots us = locate_slots(p.context_lens, p.batch, p.num_kv_heads,
+                                          p.num_splits, p.max_context, p.q_len, unit, false);
         combine_item(c, r, quarter, unit / p.num_kv_heads, unit % p.num_kv_heads,
-                     threadIdx.x % kCombineThreads, 1 + half, sh, it == first ? n_first : -1);
+                     threadIdx.x % kCombineThreads, 1 + half, sh, us.first, us.count, us.n);
     }
 }
 
@@ -350,31 +348,32 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     Small& sm = *reinterpret_cast<Small*>(smem + C::kOffSmall);
     constexpr int SN = C::SN;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int R = p.rows, G = p.group, P = p.page_size;
 
-    // The split's key range follows from the context length, one load away. The range that a
-    // context of max_context keys gives is known now, and it is the actual range whenever the
-    // split size comes out the same (split sizes are whole tiles, so any context close to
-    // max_context): thread c looks up chunk c of that range while the length is in flight, and
-    // the row cache below takes it if the sizes agree.
+    // This CTA's workspace slot, and which (sequence, KV head) unit owns it, follow from every
+    // context length (slots are shared out by length), a load away. For a batch of equal lengths
+    // slot (x, y, z) belongs to split x of KV head y of sequence z, and the split's key range is
+    // the one a context of max_context keys gives whenever the split size comes out the same
+    // (split sizes are whole tiles, so any context close to max_context): thread c looks up
+    // chunk c of that range while the lengths are in flight, and the row cache below takes it if
+    // the guess holds.
     const int per_max = keys_per_split(p.max_context, p.num_splits, p.tile_keys, p.min_split_keys);
     int page_max = 0;
-    if (tid < kRowCache && split * per_max + tid * kChunk < p.max_context)
-        page_max = p.block_table[(int64_t)b * p.max_pages_per_seq +
-                                 (split * per_max + tid * kChunk) / P];
-    int cflags;
-    const int n = clamped_context(p.context_lens, b, p.max_context, &cflags);
-    if (split == 0 && h == 0 && tid == 0) {
-        if (n < p.q_len) cflags |= DFLASH_FLAG_CONTEXT_SHORT;
-        if (cflags) atomicOr(p.status, cflags);
-    }
-    const int per = keys_per_split(n, p.num_splits, p.tile_keys, p.min_split_keys);
+    if (tid < kRowCache && blockIdx.x * per_max + tid * kChunk < p.max_context)
+        page_max = p.block_table[(int64_t)blockIdx.z * p.max_pages_per_seq +
+                                 (blockIdx.x * per_max + tid * kChunk) / P];
+    const int slot = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    const UnitSlots us = locate_slots(p.context_lens, p.batch, p.num_kv_heads, p.num_splits,
+                                      p.max_context, p.q_len, slot, true);
+    if (slot == 0 && tid == 0 && us.flags) atomicOr(p.status, us.flags);
+    const int b = us.b, h = us.h, split = slot - us.first, n = us.n;
+    const int per = b >= 0 ? keys_per_split(n, us.count, p.tile_keys, p.min_split_keys) : 1;
     const int start = split * per;
-    if (start >= n) {  // idle split: the combine never reads it
+    if (b < 0 || start >= n) {  // idle slot: the combine never reads it
         if (p.out) fused_merge<C::kThreads>(p, smem);
         return;
     }
+    const bool guessed = b == (int)blockIdx.z && split == (int)blockIdx.x && per == per_max;
     const int end = min(n, start + per);
     const int ntiles = (end - start + kTile - 1) / kTile;
     const int nvst = (end - start + kVKeys - 1) / kVKeys;
@@ -417,7 +416,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         const int nchunks = min((end - start + kChunk - 1) / kChunk, kRowCache);
         for (int c = tid; c < nchunks; c += C::kThreads) {
             const int j0 = start + c * kChunk;
-            const int phys = (per == per_max && c == tid)
+            const int phys = (guessed && c == tid)
                                  ? clamp_page(page_max, p.num_pages, &clamped)
                                  : physical_page(p.block_table, b, p.max_pages_per_seq, j0 / P,
                                                  p.num_pages, &clamped);
@@ -954,7 +953,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             }
         }
         if (alive) alive = group_sync(ctx, g, wq, epoch, false, nullptr);
-        const int64_t unit = ((int64_t)b * p.num_kv_heads + h) * p.num_splits + split;
+        const int64_t unit = slot;  // this split's workspace slot
         if (alive && !ctx.aborted()) {
 #pragma unroll
             for (int q = 0; q < kGroupRows / 2; ++q) {

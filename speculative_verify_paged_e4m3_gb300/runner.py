@@ -25,10 +25,8 @@ def algorithmic_bytes(w: W.Workload, plan) -> dict:
     kv = w.kv_bytes_per_layer()
     bt = sum(-(-n // w.page_size) for n in w.context) * 4
     q = w.batch * w.q_len * w.num_q_heads * D * 2
-    active = 0
-    for n in w.context:
-        _, a = B.dflash_verify_attn_split_bounds(plan, n)
-        active += a * w.num_kv_heads
+    _, _, act = B.dflash_verify_attn_split_slots(plan, w.context)
+    active = sum(act)
     state = active * R * (D + 2) * 4
     out = w.batch * w.q_len * w.num_q_heads * (D * 2 + 4)
     return dict(partial=kv + bt + q + state, combine=state + out, kv=kv, bt=bt, q=q,

@@ -219,3 +219,34 @@ def test_default_split_count_fills_one_wave(B):
             assert units * (plan.num_splits + 1) > plan.sm_count
         else:
             assert plan.num_splits == 1
+
+
+def test_split_slots_layout(B):
+    """Slots go to (sequence, KV head) units in proportion to length: equal lengths give
+    num_splits slots each (the [batch, Hkv, S] layout), every non-empty unit gets at least one,
+    an empty unit none, and they add up to batch * Hkv * num_splits."""
+    plan = B.dflash_verify_attn_plan(problem(B, batch=4, num_q_heads=24, num_kv_heads=4,
+                                             max_pages_per_seq=4096, num_pages=20000,
+                                             max_context=65536))
+    S, units = plan.num_splits, 16
+    start, per, act = B.dflash_verify_attn_split_slots(plan, [65536] * 4)
+    assert start == [u * S for u in range(units + 1)]
+    ref_starts, ref_active = B.dflash_verify_attn_split_bounds(plan, 65536)
+    assert all(a == ref_active for a in act) and all(p == ref_starts[1] for p in per)
+    lens = [65536, 57344, 0, 40960]
+    start, per, act = B.dflash_verify_attn_split_slots(plan, lens)
+    cnt = [start[u + 1] - start[u] for u in range(units)]
+    assert start[0] == 0 and start[-1] == units * S and all(c >= 0 for c in cnt)
+    for u in range(units):
+        n = lens[u // 4]
+        assert (cnt[u] == 0) == (n == 0) and (act[u] == 0) == (n == 0)
+        if n:
+            assert act[u] <= cnt[u] and per[u] * act[u] >= n > per[u] * (act[u] - 1)
+    share = [cnt[u] / (units * S) for u in range(units)]
+    total = 4 * sum(lens)
+    for u in range(units):
+        if lens[u // 4]:
+            assert abs(share[u] - lens[u // 4] / total) * units * S <= 1.5
+    # the longest sequence's splits are no longer than about the average
+    tiles = [math.ceil(p / 128) for p, a in zip(per, act) if a]
+    assert max(tiles) <= math.ceil(sum(math.ceil(n / 128) for n in lens) * 4 / (units * S)) + 2

@@ -256,3 +256,28 @@ def test_fused_barrier_reused_across_grid_sizes():
         torch.cuda.synchronize()
         compare(to_np(out), to_np(lse), ref_out, ref_lse, what=f"fused splits={splits}")
         assert att.workspace_views()[0].item() == 0
+
+
+def test_ragged_batch_slots_match_host_layout():
+    """A ragged batch (one sequence empty): the partial kernel writes state into exactly the
+    slots the host-side layout (dflash_verify_attn_split_slots) lists, and nothing else."""
+    from speculative_verify_paged_e4m3_gb300 import binding as B
+    w = small("slots", [3000, 700, 0, 1600], Hq=12, Hkv=2, seed=51)
+    inp = W.make_layer(w, 0, device="cpu")
+    dev = to_device(inp)
+    q = dev["q"]
+    att = B.VerifyAttention(q.shape[0], q.shape[1], q.shape[2], 2, 256, 16,
+                            dev["block_table"].shape[1], dev["k_pool"].shape[0], w.max_ctx,
+                            device=0)
+    _, state, _ = att.workspace_views()
+    state.fill_(float("nan"))
+    B.dflash_verify_attn_run(att.plan, dev["q"], dev["k_pool"], dev["v_pool"],
+                             dev["block_table"], dev["context_lens"], dev["k_scale"],
+                             dev["v_scale"], att.workspace)
+    torch.cuda.synchronize()
+    start, per, act = B.dflash_verify_attn_split_slots(att.plan, w.context)
+    written = ~torch.isnan(state[..., 1]).reshape(-1, att.plan.rows).all(dim=1).cpu().numpy()
+    want = np.zeros(written.shape, dtype=bool)
+    for u in range(len(act)):
+        want[start[u]:start[u] + act[u]] = True
+    assert np.array_equal(written, want), (np.nonzero(written != want), start, act)
