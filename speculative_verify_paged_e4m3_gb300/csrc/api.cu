@@ -210,16 +210,25 @@ int dflash_verify_attn_split_slots(const dflash_verify_attn_plan_t* plan,
         E += g[b] > 0 ? Hkv : 0;
     }
     const int64_t slots = (int64_t)B * Hkv * plan->num_splits;
-    int64_t g_before = 0, e_before = 0;
+    // one slot per non-empty unit, the rest in proportion to each unit's length beyond one even
+    // share G / slots (common.cuh, locate_slots)
+    std::vector<int64_t> x(B);
+    int64_t X = 0;
+    for (int b = 0; b < B; ++b) {
+        x[b] = g[b] > 0 && slots * g[b] > G ? slots * g[b] - G : 0;
+        X += x[b] * Hkv;
+    }
+    int64_t x_before = 0, e_before = 0;
     for (int b = 0; b < B; ++b) {
         for (int h = 0; h < Hkv; ++h) {
             const int u = b * Hkv + h;
-            slot_start[u] = G == 0 ? 0 : (int32_t)(e_before + (slots - E) * g_before / G);
-            g_before += g[b];
+            slot_start[u] =
+                G == 0 ? 0 : (int32_t)(e_before + (X > 0 ? (slots - E) * x_before / X : 0));
+            x_before += x[b];
             e_before += g[b] > 0 ? 1 : 0;
         }
     }
-    slot_start[B * Hkv] = G == 0 ? 0 : (int32_t)slots;
+    slot_start[B * Hkv] = G == 0 ? 0 : (int32_t)(E + (X > 0 ? slots - E : 0));
     for (int b = 0; b < B; ++b) {
         for (int h = 0; h < Hkv; ++h) {
             const int u = b * Hkv + h;

@@ -86,13 +86,15 @@ __device__ __forceinline__ int physical_page(const int32_t* block_table, int b,
 
 // ---- split slots of a batch -------------------------------------------------------------------
 // The plan's batch * Hkv * S split slots (one CTA each) are shared out among the (sequence, KV
-// head) units in proportion to their context lengths counted in 128-key granules: unit
+// head) units by context length, counted in 128-key granules w_u: every non-empty unit owns one
+// slot, and the other C - E slots (C slots, E non-empty units) go in proportion to each unit's
+// length beyond one even share W / C (W granules in all), x_u = max(C w_u - W, 0). Unit
 // u = b * Hkv + h owns the contiguous slots [start(u), start(u + 1)) with
-//   start(u) = (non-empty units before u) + floor((C - E) * (granules of the units before u) / W)
-// (C slots, E non-empty units, W granules of all units), so that every non-empty unit owns at
-// least one slot, an empty unit none, and units of equal length own S slots each (the
-// [batch, Hkv, S] layout). dflash_verify_attn_split_slots does the same integer arithmetic on
-// the host.
+//   start(u) = (non-empty units before u) + floor((C - E) * (x of the units before u) / X)
+// (X = sum of x; when X is 0 every non-empty unit owns one slot and the rest stay idle). A unit
+// at least one even share long then gets splits of about W / C granules, the same for all; an
+// empty unit owns no slot; units of equal length own S slots each (the [batch, Hkv, S] layout).
+// dflash_verify_attn_split_slots does the same integer arithmetic on the host.
 struct UnitSlots {
     int b, h;    // the unit (b = -1: no unit owns the slot)
     int first;   // its first slot
@@ -163,15 +165,25 @@ __device__ __forceinline__ UnitSlots locate_slots_batch_body(const int32_t* cont
     if (W == 0) return r;
     W *= Hkv;
     E *= Hkv;
-    const long long rest = (long long)B * Hkv * S - E;
-    long long w_carry = 0;
+    const long long C = (long long)B * Hkv * S;
+    const long long rest = C - E;
+    auto excess = [&](int w) { return w > 0 && C * w > W ? C * w - W : 0ll; };
+    long long X = 0;
+    for (int b0 = 0; b0 < B; b0 += 32) {
+        int unused = 0;
+        X += b0 + lane < B ? excess(slot_granules(length(b0 + lane, &unused))) : 0;
+    }
+    for (int o = 16; o > 0; o >>= 1) X += __shfl_xor_sync(0xffffffffu, X, o);
+    X *= Hkv;
+    long long x_carry = 0;
     int e_carry = 0;
     for (int b0 = 0; b0 < B; b0 += 32) {
         const int b = b0 + lane;
         int unused = 0;
         const int n = b < B ? length(b, &unused) : 0;
         const int w = slot_granules(n);
-        long long sw = w;  // inclusive scans over the chunk
+        const long long x = excess(w);
+        long long sw = x;  // inclusive scans over the chunk
         int se = w > 0;
         for (int o = 1; o < 32; o <<= 1) {
             const long long tw = __shfl_up_sync(0xffffffffu, sw, o);
@@ -181,40 +193,41 @@ __device__ __forceinline__ UnitSlots locate_slots_batch_body(const int32_t* cont
                 se += te;
             }
         }
-        const long long w_before = w_carry + sw - w;  // granules of the sequences before b
+        const long long x_before = x_carry + sw - x;  // excess of the sequences before b
         const int e_before = e_carry + se - (w > 0);   // non-empty sequences before b
-        // slot h of sequence b starts at
-        auto start = [&](long long wb0, int eb0, int wb, int hh) {
-            return (long long)Hkv * eb0 + (wb > 0 ? hh : 0) +
-                   rest * ((long long)Hkv * wb0 + (long long)hh * wb) / W;
+        // slot h of sequence b (excess xb per KV head) starts at
+        auto start = [&](long long xb0, int eb0, bool nonempty, long long xb, int hh) {
+            return (long long)Hkv * eb0 + (nonempty ? hh : 0) +
+                   (X > 0 ? rest * ((long long)Hkv * xb0 + (long long)hh * xb) / X : 0);
         };
         bool mine;
         if (by_slot)
-            mine = b < B && w > 0 && key >= start(w_before, e_before, w, 0) &&
-                   key < start(w_before, e_before, w, Hkv);
+            mine = b < B && w > 0 && key >= start(x_before, e_before, true, x, 0) &&
+                   key < start(x_before, e_before, true, x, Hkv);
         else
             mine = b == key / Hkv;
         const unsigned m = __ballot_sync(0xffffffffu, mine);
         if (m) {
             const int src = __ffs(m) - 1;
-            const long long wb0 = __shfl_sync(0xffffffffu, w_before, src);
+            const long long xb0 = __shfl_sync(0xffffffffu, x_before, src);
             const int eb0 = __shfl_sync(0xffffffffu, e_before, src);
-            const int wb = __shfl_sync(0xffffffffu, w, src);
+            const long long xb = __shfl_sync(0xffffffffu, x, src);
             const int nb = __shfl_sync(0xffffffffu, n, src);
+            const bool nonempty = nb > 0;
             int hh = 0;
             if (by_slot) {
-                while (hh + 1 < Hkv && start(wb0, eb0, wb, hh + 1) <= key) ++hh;
+                while (hh + 1 < Hkv && start(xb0, eb0, nonempty, xb, hh + 1) <= key) ++hh;
             } else {
                 hh = key % Hkv;
             }
             r.b = b0 + src;
             r.h = hh;
-            r.first = (int)start(wb0, eb0, wb, hh);
-            r.count = (int)(start(wb0, eb0, wb, hh + 1) - r.first);
+            r.first = (int)start(xb0, eb0, nonempty, xb, hh);
+            r.count = (int)(start(xb0, eb0, nonempty, xb, hh + 1) - r.first);
             r.n = nb;
             return r;
         }
-        w_carry += __shfl_sync(0xffffffffu, sw, 31);
+        x_carry += __shfl_sync(0xffffffffu, sw, 31);
         e_carry += __shfl_sync(0xffffffffu, se, 31);
     }
     return r;
