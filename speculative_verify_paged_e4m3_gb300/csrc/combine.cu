@@ -1,28 +1,36 @@
-// combine.cu -- standalone merge kernels: one CTA of 256 threads per (query row, quarter of the
-// head dim, sequence x KV head); the merge itself is combine_item (combine_impl.cuh). A single
-// sequence (every KV head owns num_splits slots) and a batch (slots shared out by length) have a
-// kernel each, so that the one-sequence kernel carries no slot search.
+// combine.cu -- standalone merge kernels, 256 threads per CTA, shaped by the split count per
+// (sequence, KV head) unit: up to 16 splits, 4 query rows per CTA with one thread per float4
+// column (combine_rows_kernel); up to 64, one row per CTA with 4 split lanes; beyond, a quarter
+// row per CTA with 16 split lanes (combine_lanes_kernel, merge in combine_item). A single
+// sequence (every KV head owns num_splits slots) and a batch (slots shared out by length) get
+// separate instances, so that the one-sequence kernels carry no slot search.
 #include "combine_impl.cuh"
 
 namespace dflash {
 
-// One sequence: every KV head owns num_splits slots, unit h at h * num_splits.
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineParams p) {
+// Split-lane items: SL split lanes x 256 / SL float4 columns, one CTA per (query row, column
+// block, unit), SL / 4 column blocks per row. 16 lanes (quarter rows) for long split lists
+// (a single long sequence: about ten splits per lane); 4 lanes (whole rows) for 17..64 splits per
+// unit (e.g. whole-model heads), so that each lane still folds about as many.
+template <int SL, bool kBatch>
+__global__ void __launch_bounds__(kCombineThreads) combine_lanes_kernel(CombineParams p) {
     __shared__ CombineScratch sh;
-    const int h = blockIdx.z;
-    int n = p.context_lens[0];
-    n = n > p.max_context ? p.max_context : (n < 0 ? 0 : n);
-    combine_item(p, blockIdx.x, blockIdx.y, 0, h, threadIdx.x, 0, sh, h * p.num_splits,
-                 p.num_splits, n);
-}
-
-// Several sequences: the unit's slots follow from every context length (locate_slots).
-__global__ void __launch_bounds__(kCombineThreads) combine_batch_kernel(CombineParams p) {
-    __shared__ CombineScratch sh;
-    const int b = blockIdx.z / p.num_kv_heads, h = blockIdx.z % p.num_kv_heads;
-    const UnitSlots us = locate_slots(p.context_lens, p.batch, p.num_kv_heads, p.num_splits,
-                                      p.max_context, p.q_len, blockIdx.z, false);
-    combine_item(p, blockIdx.x, blockIdx.y, b, h, threadIdx.x, 0, sh, us.first, us.count, us.n);
+    const int unit = blockIdx.z;
+    const int b = unit / p.num_kv_heads, h = unit % p.num_kv_heads;
+    int first, count, n;
+    if constexpr (kBatch) {  // several sequences: the unit's slots follow from every length
+        const UnitSlots us = locate_slots(p.context_lens, p.batch, p.num_kv_heads, p.num_splits,
+                                          p.max_context, p.q_len, unit, false);
+        first = us.first;
+        count = us.count;
+        n = us.n;
+    } else {  // one sequence: every KV head owns num_splits slots, unit h at h * num_splits
+        n = p.context_lens[0];
+        n = n > p.max_context ? p.max_context : (n < 0 ? 0 : n);
+        first = h * p.num_splits;
+        count = p.num_splits;
+    }
+    combine_item<SL>(p, blockIdx.x, blockIdx.y, b, h, threadIdx.x, 0, sh, first, count, n);
 }
 
 // Plans with few splits per unit (many units: a batch, whole-model heads) merge a whole row per
@@ -98,21 +106,29 @@ __global__ void __launch_bounds__(kCombineThreads) combine_rows_kernel(CombinePa
     if (col == 0) p.lse[orow] = (M == -INFINITY) ? -INFINITY : (M + log2f(Lt)) * kLn2;
 }
 
+template <int SL>
+static void launch_lanes(const CombineParams& p, cudaStream_t stream) {
+    const dim3 grid(p.rows, SL / 4, p.batch * p.num_kv_heads);
+    if (p.batch == 1)
+        combine_lanes_kernel<SL, false><<<grid, kCombineThreads, 0, stream>>>(p);
+    else
+        combine_lanes_kernel<SL, true><<<grid, kCombineThreads, 0, stream>>>(p);
+}
+
+constexpr int kMidKernelMaxSplits = 64;
+
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
-    const int units = p.batch * p.num_kv_heads;
     if (p.num_splits <= kRowKernelMaxSplits) {
-        const dim3 grid((p.rows + kRowsPerCta - 1) / kRowsPerCta, units);
+        const dim3 grid((p.rows + kRowsPerCta - 1) / kRowsPerCta, p.batch * p.num_kv_heads);
         if (p.batch == 1)
             combine_rows_kernel<false><<<grid, kCombineThreads, 0, stream>>>(p);
         else
             combine_rows_kernel<true><<<grid, kCombineThreads, 0, stream>>>(p);
-        return cudaGetLastError();
+    } else if (p.num_splits <= kMidKernelMaxSplits) {
+        launch_lanes<4>(p, stream);
+    } else {
+        launch_lanes<kCombineSplitLanes>(p, stream);
     }
-    dim3 grid(p.rows, kHeadDim / (4 * kCombineCols), units);
-    if (p.batch == 1)
-        combine_kernel<<<grid, kCombineThreads, 0, stream>>>(p);
-    else
-        combine_batch_kernel<<<grid, kCombineThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

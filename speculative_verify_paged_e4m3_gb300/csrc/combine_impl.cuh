@@ -23,27 +23,33 @@ constexpr int kCombineSplitLanes = 16;  // splits in flight per item
 constexpr int kCombineCols = 16;        // float4 columns per item (64 head-dim elements)
 constexpr int kCombineFold = 10;        // splits per lane whose loads are in flight together
 
+// Split lanes x float4 columns = the 256 threads of an item; kCombineSplitLanes lanes of
+// kCombineCols columns (a quarter of the head dim) by default.
 struct CombineScratch {
-    float4 part[kCombineSplitLanes][kCombineCols];
-    float2 ml[kCombineSplitLanes];  // (running max, running sum) of each split lane
+    float4 part[kCombineThreads];             // [split lane][column]
+    float2 ml[kCombineSplitLanes];            // (running max, running sum) of each split lane
 };
 
 __device__ __forceinline__ void combine_sync(int bar_id) {
     asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(kCombineThreads) : "memory");
 }
 
-// Merge item (row r, head-dim quarter, sequence b, KV head h). tid in [0, 256) indexes the 256
-// threads that share named barrier bar_id and scratch sh. Each split lane folds its splits
-// (sl, sl + 16, ...) into a running (max, sum, numerator) in one pass, so that all its loads can
-// be in flight at once; the 16 lanes are then merged the same way through shared memory. The split
-// state is read through L2 (ld.global.cg), so that state written by other CTAs of the same launch
-// is seen.
+// Merge item (row r, column block cb of the head dim, sequence b, KV head h) with SL split lanes
+// of 256 / SL float4 columns (block cb covers head-dim elements [cb, cb + 1) x 1024 / SL). tid
+// in [0, 256) indexes the 256 threads that share named barrier bar_id and scratch sh. Each split
+// lane folds its splits (sl, sl + SL, ...) into a running (max, sum, numerator) in one pass, so
+// that all its loads can be in flight at once; the lanes are then merged the same way through
+// shared memory. The split state is read through L2 (ld.global.cg), so that state written by
+// other CTAs of the same launch is seen.
 // The unit's splits sit in workspace slots [first, first + count) (common.cuh, locate_slots);
 // n is its context length (clamped).
+template <int SL = kCombineSplitLanes>
 __device__ __forceinline__ void combine_item(const CombineParams& p, int r, int quarter, int b,
                                              int h, int tid, int bar_id, CombineScratch& sh,
                                              int first, int count, int n) {
-    const int sl = tid / kCombineCols, col = tid % kCombineCols;
+    constexpr int kCols = kCombineThreads / SL;
+    static_assert(SL <= kCombineSplitLanes && kCols * SL == kCombineThreads, "item shape");
+    const int sl = tid / kCols, col = tid % kCols;
     n = count > 0 ? n : 0;
     const int per = n > 0 ? keys_per_split(n, count, p.tile_keys, p.min_split_keys) : 1;
     const int active = n > 0 ? (n + per - 1) / per : 0;
@@ -53,7 +59,7 @@ __device__ __forceinline__ void combine_item(const CombineParams& p, int r, int 
 
     float m = -INFINITY, L = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = sl; s0 < active; s0 += kCombineSplitLanes * kCombineFold) {
+    for (int s0 = sl; s0 < active; s0 += SL * kCombineFold) {
         // all loads of kCombineFold splits first (one round trip), then the fold; an active split
         // always has its numerator written (zero for a row it does not see)
         float2 st[kCombineFold];
@@ -61,13 +67,13 @@ __device__ __forceinline__ void combine_item(const CombineParams& p, int r, int 
 #pragma unroll
         for (int k = 0; k < kCombineFold; ++k) {
             // unconditional loads (index clamped into the allocation), masked afterwards
-            const int s = min(s0 + k * kCombineSplitLanes, active - 1);
+            const int s = min(s0 + k * SL, active - 1);
             st[k] = __ldcg(&p.ws_state[(base + s) * R + r]);
-            a[k] = __ldcg(&acc4[((base + s) * R + r) * (kHeadDim / 4) + quarter * kCombineCols + col]);
+            a[k] = __ldcg(&acc4[((base + s) * R + r) * (kHeadDim / 4) + quarter * kCols + col]);
         }
 #pragma unroll
         for (int k = 0; k < kCombineFold; ++k) {
-            if (s0 + k * kCombineSplitLanes >= active) {
+            if (s0 + k * SL >= active) {
                 st[k] = make_float2(-INFINITY, 0.f);
                 a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
@@ -82,21 +88,21 @@ __device__ __forceinline__ void combine_item(const CombineParams& p, int r, int 
             m = mn;
         }
     }
-    sh.part[sl][col] = o;
+    sh.part[sl * kCols + col] = o;
     if (col == 0) sh.ml[sl] = make_float2(m, L);
     combine_sync(bar_id);
-    if (tid < kCombineCols) {
+    if (tid < kCols) {
         float M = -INFINITY;
 #pragma unroll
-        for (int k = 0; k < kCombineSplitLanes; ++k) M = fmaxf(M, sh.ml[k].x);
+        for (int k = 0; k < SL; ++k) M = fmaxf(M, sh.ml[k].x);
         float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
         float Lt = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
-            for (int k = 0; k < kCombineSplitLanes; ++k) {
+            for (int k = 0; k < SL; ++k) {
                 const float2 ml = sh.ml[k];
                 const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-                const float4 q = sh.part[k][tid];
+                const float4 q = sh.part[k * kCols + tid];
                 t.x = fmaf(w, q.x, t.x);
                 t.y = fmaf(w, q.y, t.y);
                 t.z = fmaf(w, q.z, t.z);
@@ -111,7 +117,7 @@ __device__ __forceinline__ void combine_item(const CombineParams& p, int r, int 
         const int i = r / p.group, g = r % p.group;
         const int64_t orow = ((int64_t)b * p.q_len + i) * p.num_q_heads + h * p.group + g;
         __half2* out2 =
-            reinterpret_cast<__half2*>(p.out + orow * kHeadDim + (quarter * kCombineCols + tid) * 4);
+            reinterpret_cast<__half2*>(p.out + orow * kHeadDim + (quarter * kCols + tid) * 4);
         out2[0] = __floats2half2_rn(t.x, t.y);
         out2[1] = __floats2half2_rn(t.z, t.w);
         if (quarter == 0 && tid == 0)
