@@ -301,23 +301,44 @@ def run_ours(args, rank, world, local_rank):
     # the outputs and LSEs; the KV cache stays resident (it is the model's state, not an input)
     e2e = None
     if not args.no_e2e:
-        host_in = [{k: lay[k].cpu().pin_memory() for k in
-                    ("q", "block_table", "context_lens", "k_scale", "v_scale")}
-                   for lay in stack.layers]
-        host_out = [(o.cpu().pin_memory(), l.cpu().pin_memory())
-                    for o, l in zip(stack.outs, stack.lses)]
-        h2d = sum(t.numel() * t.element_size() for d in host_in for t in d.values())
-        d2h = sum(o.numel() * o.element_size() + l.numel() * l.element_size()
-                  for o, l in host_out)
+        # one pinned buffer per direction: every layer's inputs (Q, block table, context length,
+        # scales) go up in one copy, every layer's out and lse come back in one copy; the layer
+        # tensors become views of the device-side buffers, so the forward reads and writes them
+        # in place
+        keys = ("q", "block_table", "context_lens", "k_scale", "v_scale")
+
+        def layout(tensors):
+            offs, total = [], 0
+            for t in tensors:
+                total = (total + 255) // 256 * 256
+                offs.append(total)
+                total += t.numel() * t.element_size()
+            return offs, total
+
+        def view(buf, off, t):
+            return buf[off:off + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+
+        ins = [(lay, k) for lay in stack.layers for k in keys]
+        in_offs, in_total = layout([lay[k] for lay, k in ins])
+        dev_in = torch.empty(in_total, dtype=torch.uint8, device=dev)
+        host_in = torch.empty(in_total, dtype=torch.uint8).pin_memory()
+        for (lay, k), off in zip(ins, in_offs):
+            view(host_in, off, lay[k]).copy_(lay[k].cpu())
+            v = view(dev_in, off, lay[k])
+            v.copy_(lay[k])
+            lay[k] = v
+        outs = [t for pair in zip(stack.outs, stack.lses) for t in pair]
+        out_offs, out_total = layout(outs)
+        dev_out = torch.empty(out_total, dtype=torch.uint8, device=dev)
+        host_out = torch.empty(out_total, dtype=torch.uint8).pin_memory()
+        views = [view(dev_out, off, t) for t, off in zip(outs, out_offs)]
+        stack.outs, stack.lses = views[0::2], views[1::2]
+        h2d, d2h = in_total, out_total
 
         def e2e_step():
-            for lay, hin in zip(stack.layers, host_in):
-                for k, t in hin.items():
-                    lay[k].copy_(t, non_blocking=True)
+            dev_in.copy_(host_in, non_blocking=True)
             stack.launch()
-            for (o, l), (ho, hl) in zip(zip(stack.outs, stack.lses), host_out):
-                ho.copy_(o, non_blocking=True)
-                hl.copy_(l, non_blocking=True)
+            host_out.copy_(dev_out, non_blocking=True)
 
         for _ in range(max(1, args.warmup)):
             e2e_step()
