@@ -66,7 +66,7 @@
 extern "C" {
 #endif
 
-#define DFLASH_VERIFY_ATTN_VERSION 1
+#define DFLASH_VERIFY_ATTN_VERSION 2
 
 typedef enum {
     DFLASH_OK = 0,
@@ -94,9 +94,9 @@ typedef enum {
 typedef struct {
     int32_t version;           /* DFLASH_VERIFY_ATTN_VERSION */
     int32_t batch;             /* sequences, >= 1 */
-    int32_t q_len;             /* drafted tokens per sequence, 1..8 */
+    int32_t q_len;             /* drafted tokens per sequence, >= 1 (8 in the pages' runs) */
     int32_t num_q_heads;       /* Hq */
-    int32_t num_kv_heads;      /* Hkv; Hq % Hkv == 0 and q_len * Hq / Hkv <= 64 */
+    int32_t num_kv_heads;      /* Hkv; Hq % Hkv == 0 and R = q_len * Hq / Hkv <= 256 */
     int32_t head_dim;          /* 256 */
     int32_t page_size;         /* tokens per page; a multiple of 16 */
     int32_t max_pages_per_seq; /* block-table row stride; >= ceil(max_context / page_size) */
@@ -120,6 +120,9 @@ typedef struct {
     int32_t smem_bytes;       /* partial-kernel dynamic shared memory */
     int32_t sm_count;         /* SMs of plan.problem.device */
     int32_t combine_fused;    /* 1: forward merges the splits inside the partial-kernel launch */
+    int32_t row_blocks;       /* CTAs per split, each carrying ceil(R / row_blocks) consecutive
+                                 rows (1 unless R exceeds what one CTA of the kernel holds: 48
+                                 rows for TCGEN05, 64 for SIMT) */
     size_t workspace_bytes;   /* caller allocates at least this many bytes */
     size_t ws_state_offset;   /* float2 (m, l) [slots, R]; m in log2 units (slots below) */
     size_t ws_acc_offset;     /* float numerator [slots, R, head_dim], v_scale applied */

@@ -15,7 +15,7 @@ import torch
 
 from . import build as _build
 
-DFLASH_VERIFY_ATTN_VERSION = 1
+DFLASH_VERIFY_ATTN_VERSION = 2
 DFLASH_OK = 0
 DFLASH_ERR_INVALID_ARGUMENT = -1
 DFLASH_ERR_UNSUPPORTED = -2
@@ -54,7 +54,7 @@ class Problem(ctypes.Structure):
 class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "version", "kernel", "num_splits", "tile_keys", "min_split_keys", "rows", "threads",
-        "smem_bytes", "sm_count", "combine_fused")] + [
+        "smem_bytes", "sm_count", "combine_fused", "row_blocks")] + [
         ("workspace_bytes", ctypes.c_size_t),
         ("ws_state_offset", ctypes.c_size_t),
         ("ws_acc_offset", ctypes.c_size_t),

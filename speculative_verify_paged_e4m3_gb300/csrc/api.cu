@@ -29,6 +29,8 @@ size_t simt_smem_bytes();
 size_t tc_smem_bytes(int rows);
 int tc_threads(int rows);
 bool tc_supports(int rows);
+int tc_max_rows();
+int simt_max_rows();
 }  // namespace dflash
 
 using namespace dflash;
@@ -53,7 +55,13 @@ int host_keys_per_split(int n, const dflash_verify_attn_plan_t* plan) {
 
 int check_plan(const dflash_verify_attn_plan_t* plan) {
     if (!plan || plan->version != DFLASH_VERIFY_ATTN_VERSION) return DFLASH_ERR_INVALID_ARGUMENT;
-    if (plan->num_splits < 1 || plan->tile_keys < 1 || plan->rows < 1)
+    if (plan->num_splits < 1 || plan->tile_keys < 1 || plan->rows < 1 || plan->row_blocks < 1 ||
+        plan->row_blocks > plan->rows)
+        return DFLASH_ERR_INVALID_ARGUMENT;
+    // every row block holds 1..capacity rows of the plan's kernel
+    const int64_t block_rows = ceil_div(plan->rows, plan->row_blocks);
+    const int capacity = plan->kernel == DFLASH_KERNEL_TCGEN05 ? tc_max_rows() : simt_max_rows();
+    if (block_rows > capacity || (plan->row_blocks - 1) * block_rows >= plan->rows)
         return DFLASH_ERR_INVALID_ARGUMENT;
     return DFLASH_OK;
 }
@@ -81,6 +89,8 @@ PartialParams partial_params(const dflash_verify_attn_plan_t* plan, const void* 
     p.num_kv_heads = pr.num_kv_heads;
     p.group = pr.num_q_heads / pr.num_kv_heads;
     p.rows = plan->rows;
+    p.row_blocks = plan->row_blocks;
+    p.block_rows = (int)ceil_div(plan->rows, plan->row_blocks);
     p.page_size = pr.page_size;
     p.max_pages_per_seq = pr.max_pages_per_seq;
     p.num_pages = pr.num_pages;
@@ -127,9 +137,16 @@ int dflash_verify_attn_plan(const dflash_verify_attn_problem* pr,
     const int group = pr->num_q_heads / pr->num_kv_heads;
     const int64_t rows = (int64_t)pr->q_len * group;
     if (rows > kMaxRows) return DFLASH_ERR_UNSUPPORTED;
-    const bool tc_ok = tc_supports((int)rows);
+    // More rows than one CTA of the chosen kernel carries: the rows are dealt into row blocks of
+    // ceil(R / blocks) each, every block a CTA of its own over the same split (the split count
+    // shrinks by the same factor, so the grid stays one wave).
+    const int tc_blocks = (int)ceil_div(rows, tc_max_rows());
+    const int tc_block_rows = (int)ceil_div(rows, tc_blocks);
+    const bool tc_ok = tc_supports(tc_block_rows);
     if (pr->kernel == DFLASH_KERNEL_TCGEN05 && !tc_ok) return DFLASH_ERR_UNSUPPORTED;
     const bool use_tc = tc_ok && pr->kernel != DFLASH_KERNEL_SIMT;
+    const int row_blocks = use_tc ? tc_blocks : (int)ceil_div(rows, simt_max_rows());
+    const int block_rows = (int)ceil_div(rows, row_blocks);
 
     int sm_count = kDefaultSmCount;
     if (pr->device >= 0) {
@@ -146,8 +163,8 @@ int dflash_verify_attn_plan(const dflash_verify_attn_problem* pr,
         plan->kernel = DFLASH_KERNEL_TCGEN05;
         plan->tile_keys = 128;
         plan->min_split_keys = 256;
-        plan->threads = tc_threads((int)rows);
-        plan->smem_bytes = (int32_t)tc_smem_bytes((int)rows);
+        plan->threads = tc_threads(block_rows);
+        plan->smem_bytes = (int32_t)tc_smem_bytes(block_rows);
     } else {
         plan->kernel = DFLASH_KERNEL_SIMT;
         plan->tile_keys = 32;
@@ -156,21 +173,22 @@ int dflash_verify_attn_plan(const dflash_verify_attn_problem* pr,
         plan->smem_bytes = (int32_t)simt_smem_bytes();
     }
     const int64_t units = (int64_t)pr->batch * pr->num_kv_heads;
+    const int64_t ctas_per_split = units * row_blocks;  // CTAs per split index
     // On request the tensor-core kernel merges the splits itself (one launch per forward), which
     // needs its whole grid on the GPU at once (one CTA per SM): the split count is then kept to
-    // floor(SMs / units).
+    // floor(SMs / (units * row blocks)).
     const bool fuse = use_tc && (pr->flags & DFLASH_PROBLEM_FUSED_COMBINE) &&
-                      units <= sm_count &&
-                      (pr->num_splits == 0 || units * pr->num_splits <= sm_count);
+                      ctas_per_split <= sm_count &&
+                      (pr->num_splits == 0 || ctas_per_split * pr->num_splits <= sm_count);
     int64_t S = pr->num_splits;
     if (S == 0 && fuse) {
-        S = sm_count / units;
+        S = sm_count / ctas_per_split;
         const int64_t cap = ceil_div(pr->max_context, plan->min_split_keys);
         if (S > cap) S = cap;
     } else if (S == 0) {
-        // one wave of single-CTA-per-SM work: units * S <= SMs (a CTA past the SM count would
-        // wait for a second wave and double the launch time)
-        S = units < sm_count ? sm_count / units : 1;
+        // one wave of single-CTA-per-SM work: units * row blocks * S <= SMs (a CTA past the SM
+        // count would wait for a second wave and double the launch time)
+        S = ctas_per_split < sm_count ? sm_count / ctas_per_split : 1;
         const int64_t cap = ceil_div(pr->max_context, plan->min_split_keys);
         if (S > cap) S = cap;
     }
@@ -179,6 +197,7 @@ int dflash_verify_attn_plan(const dflash_verify_attn_problem* pr,
     plan->num_splits = (int32_t)S;
     plan->combine_fused = fuse ? 1 : 0;
     plan->rows = (int32_t)rows;
+    plan->row_blocks = row_blocks;
     plan->sm_count = sm_count;
     const size_t state_bytes = (size_t)units * S * rows * sizeof(float2);
     const size_t acc_bytes = (size_t)units * S * rows * kHeadDim * sizeof(float);

@@ -9,7 +9,7 @@
 namespace dflash {
 
 constexpr int kHeadDim = 256;  // the only head dim the kernels are built for
-constexpr int kMaxRows = 64;   // q_len * Hq / Hkv rows per KV head a CTA carries
+constexpr int kMaxRows = 256;  // q_len * Hq / Hkv rows per KV head (split over row blocks)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -27,6 +27,9 @@ struct PartialParams {
     int batch, q_len, num_q_heads, num_kv_heads, group, rows;
     int page_size, max_pages_per_seq, num_pages, max_context;
     int num_splits, tile_keys, min_split_keys;
+    // Row blocks: the grid's x extent is num_splits * row_blocks; CTA x = split * row_blocks + k
+    // carries rows [k * block_rows, min(rows, (k + 1) * block_rows)) of that split's slot.
+    int row_blocks, block_rows;
     // merge of the splits inside the same launch (every CTA resident): grid barrier words in the
     // workspace header, then FP16 output and FP32 log-sum-exp; null out when not fused
     unsigned long long* grid_bar;  // ticket counter of the grid barrier (workspace header)
@@ -43,6 +46,32 @@ struct CombineParams {
     int batch, q_len, num_q_heads, num_kv_heads, group, rows;
     int max_context, num_splits, tile_keys, min_split_keys;
 };
+
+// This CTA's place in a row-blocked grid: the split position x / row_blocks (the workspace slot
+// is that position plus num_splits per (KV head, sequence) grid row) and its row range.
+struct RowBlock {
+    int xs;      // split position within the grid row
+    int slot;    // workspace slot
+    int row_lo;  // first row (of R) this CTA carries
+    int rows;    // rows it carries, >= 1
+};
+
+// Host check of a launch's row blocks: every block carries 1..capacity rows and together they
+// cover the R rows exactly once.
+inline bool row_blocks_valid(const PartialParams& p, int capacity) {
+    return p.row_blocks >= 1 && p.block_rows >= 1 && p.block_rows <= capacity &&
+           (int64_t)p.row_blocks * p.block_rows >= p.rows &&
+           (int64_t)(p.row_blocks - 1) * p.block_rows < p.rows;
+}
+
+__device__ __forceinline__ RowBlock row_block(const PartialParams& p) {
+    RowBlock rb;
+    rb.xs = blockIdx.x / p.row_blocks;
+    rb.row_lo = (blockIdx.x - rb.xs * p.row_blocks) * p.block_rows;
+    rb.rows = min(p.block_rows, p.rows - rb.row_lo);
+    rb.slot = rb.xs + p.num_splits * (blockIdx.y + gridDim.y * blockIdx.z);
+    return rb;
+}
 
 // Context length of sequence b as the kernels see it: clamped into [0, max_context].
 __device__ __forceinline__ int clamped_context(const int32_t* context_lens, int b, int max_context,

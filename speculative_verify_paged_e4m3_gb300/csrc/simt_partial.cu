@@ -1,7 +1,8 @@
 // simt_partial.cu -- CUDA-core FP32 split-KV partial attention (the correctness baseline kernel).
 //
-// One CTA per (split, KV head, sequence). It keeps every query row of its KV head (up to 64:
-// q_len x six heads in the pages' q8 / Hq6 / Hkv1 shape) against each staged K/V tile, which is
+// One CTA per (split, KV head, sequence) and row block. It keeps the query rows of its block (up
+// to 64; every row of the KV head, q_len x six heads, in the pages' q8 / Hq6 / Hkv1 shape) against
+// each staged K/V tile, which is
 // the "six-head KV reuse" of "[Perf] Reduce DFlash2 long-context verification decay",
 // Implementation, and writes the split's FP32 max / sum / numerator ("complete FP32 workspace",
 // "[Perf] Reduce DFlash2 attention cost and screen exact QK reuse", Purpose).
@@ -15,13 +16,16 @@
 namespace dflash {
 
 constexpr int kSimtThreads = 256;
+constexpr int kSimtRows = 64;  // rows per row block this kernel carries
 constexpr int kSimtTile = 32;
 constexpr int kKStride = kHeadDim + 1;
 constexpr int kPStride = kSimtTile + 1;
 
+int simt_max_rows() { return kSimtRows; }
+
 size_t simt_smem_bytes() {
-    return sizeof(float) * (size_t)(kMaxRows * kHeadDim + kSimtTile * kKStride +
-                                    kSimtTile * kHeadDim + kMaxRows * kPStride + kMaxRows);
+    return sizeof(float) * (size_t)(kSimtRows * kHeadDim + kSimtTile * kKStride +
+                                    kSimtTile * kHeadDim + kSimtRows * kPStride + kSimtRows);
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -38,18 +42,17 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 __global__ void __launch_bounds__(kSimtThreads, 1) simt_partial_kernel(PartialParams p) {
     extern __shared__ float smem[];
-    float* Qs = smem;                               // [kMaxRows][kHeadDim]
-    float* Ks = Qs + kMaxRows * kHeadDim;           // [kSimtTile][kKStride]
+    float* Qs = smem;                               // [kSimtRows][kHeadDim]
+    float* Ks = Qs + kSimtRows * kHeadDim;           // [kSimtTile][kKStride]
     float* Vs = Ks + kSimtTile * kKStride;          // [kSimtTile][kHeadDim]
-    float* Ps = Vs + kSimtTile * kHeadDim;          // [kMaxRows][kPStride]
-    float* alpha_s = Ps + kMaxRows * kPStride;      // [kMaxRows]
+    float* Ps = Vs + kSimtTile * kHeadDim;          // [kSimtRows][kPStride]
+    float* alpha_s = Ps + kSimtRows * kPStride;      // [kSimtRows]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int G = p.group, R = p.rows;
-
-    // this CTA's workspace slot and the (sequence, KV head) unit owning it (slots are shared out
-    // by context length; common.cuh)
-    const int slot = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    // this CTA's workspace slot and rows, and the (sequence, KV head) unit owning the slot
+    // (slots are shared out by context length; common.cuh)
+    const RowBlock rb = row_block(p);
+    const int G = p.group, R = rb.rows, row_lo = rb.row_lo, slot = rb.slot;
     const UnitSlots us = locate_slots(p.context_lens, p.batch, p.num_kv_heads, p.num_splits,
                                       p.max_context, p.q_len, slot, true);
     if (slot == 0 && tid == 0 && us.flags) atomicOr(p.status, us.flags);
@@ -61,25 +64,25 @@ __global__ void __launch_bounds__(kSimtThreads, 1) simt_partial_kernel(PartialPa
     const int end = min(n, start + per);
 
     const float qscale = __ldg(p.k_scale) * 0.0625f * kLog2e;  // D = 256: D^-1/2 = 1/16
-    for (int idx = tid; idx < kMaxRows * kHeadDim; idx += kSimtThreads) {
+    for (int idx = tid; idx < kSimtRows * kHeadDim; idx += kSimtThreads) {
         const int r = idx / kHeadDim, d = idx % kHeadDim;
         float v = 0.f;
         if (r < R) {
-            const int i = r / G, g = r % G;
+            const int i = (row_lo + r) / G, g = (row_lo + r) % G;
             const int64_t qrow = ((int64_t)b * p.q_len + i) * p.num_q_heads + h * G + g;
             v = __half2float(p.q[qrow * kHeadDim + d]) * qscale;
         }
         Qs[idx] = v;
     }
 
-    float m_run[kMaxRows / 8], l_run[kMaxRows / 8], acc[kMaxRows];
+    float m_run[kSimtRows / 8], l_run[kSimtRows / 8], acc[kSimtRows];
 #pragma unroll
-    for (int m = 0; m < kMaxRows / 8; ++m) {
+    for (int m = 0; m < kSimtRows / 8; ++m) {
         m_run[m] = -INFINITY;
         l_run[m] = 0.f;
     }
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.f;
+    for (int r = 0; r < kSimtRows; ++r) acc[r] = 0.f;
 
     bool page_clamped = false;
     for (int t0 = start; t0 < end; t0 += kSimtTile) {
@@ -118,19 +121,19 @@ __global__ void __launch_bounds__(kSimtThreads, 1) simt_partial_kernel(PartialPa
         __syncthreads();
 
         // scores: lane = key of the tile, rows warp + 8m
-        float s[kMaxRows / 8];
+        float s[kSimtRows / 8];
 #pragma unroll
-        for (int m = 0; m < kMaxRows / 8; ++m) s[m] = 0.f;
+        for (int m = 0; m < kSimtRows / 8; ++m) s[m] = 0.f;
         for (int d = 0; d < kHeadDim; ++d) {
             const float kv = Ks[lane * kKStride + d];
 #pragma unroll
-            for (int m = 0; m < kMaxRows / 8; ++m) s[m] = fmaf(Qs[(warp + 8 * m) * kHeadDim + d], kv, s[m]);
+            for (int m = 0; m < kSimtRows / 8; ++m) s[m] = fmaf(Qs[(warp + 8 * m) * kHeadDim + d], kv, s[m]);
         }
         const int j = t0 + lane;
 #pragma unroll
-        for (int m = 0; m < kMaxRows / 8; ++m) {
+        for (int m = 0; m < kSimtRows / 8; ++m) {
             const int r = warp + 8 * m;
-            const int i = r / G;
+            const int i = (row_lo + r) / G;
             const bool valid = (r < R) && (j < end) && (j <= n - p.q_len + i);
             const float sv = valid ? s[m] : -INFINITY;
             const float mn = fmaxf(m_run[m], warp_max(sv));
@@ -148,25 +151,26 @@ __global__ void __launch_bounds__(kSimtThreads, 1) simt_partial_kernel(PartialPa
 
         // numerator: thread = head-dim element
 #pragma unroll
-        for (int r = 0; r < kMaxRows; ++r) acc[r] *= alpha_s[r];
+        for (int r = 0; r < kSimtRows; ++r) acc[r] *= alpha_s[r];
         for (int kk = 0; kk < kSimtTile; ++kk) {
             const float v = Vs[kk * kHeadDim + tid];
 #pragma unroll
-            for (int r = 0; r < kMaxRows; ++r) acc[r] = fmaf(Ps[r * kPStride + kk], v, acc[r]);
+            for (int r = 0; r < kSimtRows; ++r) acc[r] = fmaf(Ps[r * kPStride + kk], v, acc[r]);
         }
     }
     if (page_clamped) atomicOr(p.status, DFLASH_FLAG_PAGE_CLAMPED);
 
     const int64_t unit = slot;  // this split's workspace slot
 #pragma unroll
-    for (int m = 0; m < kMaxRows / 8; ++m) {
+    for (int m = 0; m < kSimtRows / 8; ++m) {
         const int r = warp + 8 * m;
-        if (r < R && lane == 0) p.ws_state[unit * R + r] = make_float2(m_run[m], l_run[m]);
+        if (r < R && lane == 0)
+            p.ws_state[unit * p.rows + row_lo + r] = make_float2(m_run[m], l_run[m]);
     }
     const float vs = __ldg(p.v_scale);
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r)
-        if (r < R) p.ws_acc[(unit * R + r) * kHeadDim + tid] = acc[r] * vs;
+    for (int r = 0; r < kSimtRows; ++r)
+        if (r < R) p.ws_acc[(unit * p.rows + row_lo + r) * kHeadDim + tid] = acc[r] * vs;
 }
 
 cudaError_t launch_simt_partial(const PartialParams& p, cudaStream_t stream) {
@@ -174,7 +178,8 @@ cudaError_t launch_simt_partial(const PartialParams& p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(simt_partial_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.num_splits, p.num_kv_heads, p.batch);
+    if (!row_blocks_valid(p, kSimtRows)) return cudaErrorInvalidValue;
+    dim3 grid(p.num_splits * p.row_blocks, p.num_kv_heads, p.batch);
     simt_partial_kernel<<<grid, kSimtThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }

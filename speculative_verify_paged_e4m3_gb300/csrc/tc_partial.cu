@@ -348,7 +348,9 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     Small& sm = *reinterpret_cast<Small*>(smem + C::kOffSmall);
     constexpr int SN = C::SN;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int R = p.rows, G = p.group, P = p.page_size;
+    // rows [row_lo, row_lo + R) of the slot: all of them unless R > 48 (row blocks)
+    const RowBlock rblk = row_block(p);
+    const int R = rblk.rows, row_lo = rblk.row_lo, G = p.group, P = p.page_size;
 
     // This CTA's workspace slot, and which (sequence, KV head) unit owns it, follow from every
     // context length (slots are shared out by length), a load away. For a batch of equal lengths
@@ -359,10 +361,10 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     // the guess holds.
     const int per_max = keys_per_split(p.max_context, p.num_splits, p.tile_keys, p.min_split_keys);
     int page_max = 0;
-    if (tid < kRowCache && blockIdx.x * per_max + tid * kChunk < p.max_context)
+    if (tid < kRowCache && rblk.xs * per_max + tid * kChunk < p.max_context)
         page_max = p.block_table[(int64_t)blockIdx.z * p.max_pages_per_seq +
-                                 (blockIdx.x * per_max + tid * kChunk) / P];
-    const int slot = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+                                 (rblk.xs * per_max + tid * kChunk) / P];
+    const int slot = rblk.slot;
     const UnitSlots us = locate_slots(p.context_lens, p.batch, p.num_kv_heads, p.num_splits,
                                       p.max_context, p.q_len, slot, true);
     if (slot == 0 && tid == 0 && us.flags) atomicOr(p.status, us.flags);
@@ -373,7 +375,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         if (p.out) fused_merge<C::kThreads>(p, smem);
         return;
     }
-    const bool guessed = b == (int)blockIdx.z && split == (int)blockIdx.x && per == per_max;
+    const bool guessed = b == (int)blockIdx.z && split == rblk.xs && per == per_max;
     const int end = min(n, start + per);
     const int ntiles = (end - start + kTile - 1) / kTile;
     const int nvst = (end - start + kVKeys - 1) / kVKeys;
@@ -679,7 +681,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         const int st = (wq << 5) | lane;  // key of the tile = tensor-memory lane
         const int row0 = kGroupRows * g;
         const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
-        const int qoff = n - p.q_len;  // row r sees keys j <= qoff + r / G
+        const int qoff = n - p.q_len;  // row r of the slot sees keys j <= qoff + r / G
 
         // Q -> three E4M3 terms (one warp per row), row scales
         {
@@ -691,7 +693,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                 const int r = sw + C::kSoftWarps * k;
                 qraw[k] = make_uint4(0, 0, 0, 0);
                 if (r < R) {
-                    const int i = r / G, gg = r % G;
+                    const int i = (row_lo + r) / G, gg = (row_lo + r) % G;
                     const int64_t qrow = ((int64_t)b * p.q_len + i) * p.num_q_heads + h * G + gg;
                     qraw[k] = *reinterpret_cast<const uint4*>(p.q + qrow * kHeadDim + lane * 8);
                 }
@@ -802,7 +804,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             if (!((tile0 + kTile <= end) && (tile0 + kTile - 1 <= qoff))) {
 #pragma unroll
                 for (int i = 0; i < kGroupRows; ++i) {
-                    const bool v = j < end && j <= qoff + (row0 + i) / G;
+                    const bool v = j < end && j <= qoff + (row_lo + row0 + i) / G;
                     if (!v) validm &= ~(1u << i);
                 }
             }
@@ -963,7 +965,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                     if (st == i && row0 + i < R) {
                         const float L = sm.rsum[g][0][i] + sm.rsum[g][1][i] + sm.rsum[g][2][i] +
                                         sm.rsum[g][3][i];
-                        p.ws_state[unit * R + row0 + i] =
+                        p.ws_state[unit * p.rows + row_lo + row0 + i] =
                             make_float2(-(k ? hi2(nm[q]) : lo2(nm[q])), L);
                     }
                 }
@@ -982,7 +984,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < kGroupRows; ++i) {
                     const int r = row0 + i;
-                    if (r < R) p.ws_acc[(unit * R + r) * kHeadDim + d] = o[i] * vs;
+                    if (r < R) p.ws_acc[(unit * p.rows + row_lo + r) * kHeadDim + d] = o[i] * vs;
                 }
             }
         }
@@ -1002,6 +1004,8 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
 int tc_rows_pad(int rows) { return (rows + tc::kGroupRows - 1) / tc::kGroupRows * tc::kGroupRows; }
 
 bool tc_supports(int rows) { return tc_rows_pad(rows) <= tc::kMaxRP; }
+
+int tc_max_rows() { return tc::kMaxRP; }
 
 size_t tc_smem_bytes(int rows) {
     switch (tc_rows_pad(rows)) {
@@ -1045,7 +1049,7 @@ static cudaError_t launch_rp(const CUtensorMap& kmap, const CUtensorMap& vmap,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.num_splits, p.num_kv_heads, p.batch);
+    cfg.gridDim = dim3(p.num_splits * p.row_blocks, p.num_kv_heads, p.batch);
     cfg.blockDim = dim3(tc::Cfg<RP>::kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -1060,8 +1064,8 @@ static cudaError_t launch_rp(const CUtensorMap& kmap, const CUtensorMap& vmap,
 }
 
 cudaError_t launch_tc_partial(const PartialParams& p, cudaStream_t stream) {
-    const int rp = tc_rows_pad(p.rows);
-    if (rp > tc::kMaxRP) return cudaErrorInvalidValue;
+    if (!row_blocks_valid(p, tc::kMaxRP)) return cudaErrorInvalidValue;
+    const int rp = tc_rows_pad(p.block_rows);
     const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     // K and V pools (rows of Hkv * 256 bytes, num_pages * page_size of them) viewed as 4-D:

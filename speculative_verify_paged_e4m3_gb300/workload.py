@@ -169,7 +169,8 @@ def config3() -> Workload:
 
 
 def config4(q_len: int, context: int) -> Workload:
-    """Tail-shape sweep point: q_len in 1..8, N in {4096, 65536, 262144}, 16 layers, page 16."""
+    """Tail-shape sweep point: q_len in 1..8 (longer drafted blocks, up to 16, take the same
+    recipe), N in {4096, 65536, 262144}, 16 layers, page 16."""
     return Workload(f"c4_q{q_len}_ctx{context}_p16", layers=16, context=(context,), q_len=q_len,
                     seed_base=40000 + 1000 * q_len + 200 * _ctx_index(context))
 

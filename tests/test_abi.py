@@ -72,7 +72,7 @@ def test_plan_q8_capacity(B):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(version=2), -1),
+    (dict(version=1), -1),
     (dict(batch=0), -1),
     (dict(q_len=0), -1),
     (dict(num_q_heads=5, num_kv_heads=2), -1),
@@ -82,14 +82,61 @@ def test_plan_q8_capacity(B):
     (dict(kernel=7), -1),
     (dict(head_dim=128), -2),
     (dict(page_size=24, max_pages_per_seq=20000), -2),
-    (dict(q_len=9, num_q_heads=8), -2),  # 72 rows per KV head
-    (dict(num_q_heads=8, kernel=2), -2),  # 64 rows: above the tensor-core kernel's 48
+    (dict(q_len=33, num_q_heads=8), -2),  # 264 rows per KV head: above 256
 ])
 def test_plan_errors(B, kw, status):
     pr = problem(B, **{k: v for k, v in kw.items() if k != "version"})
     if "version" in kw:
         pr.version = kw["version"]
     assert B.dflash_verify_attn_plan_status(pr) == status
+
+
+@pytest.mark.parametrize("q_len,hq,kernel,blocks,block_rows,threads_of", [
+    (8, 6, 0, 1, 48, 48),     # the pages' shape: one CTA per split
+    (9, 6, 0, 2, 27, 32),     # 54 rows: two blocks of 27 on the 32-row instance
+    (10, 6, 0, 2, 30, 32),
+    (16, 6, 0, 2, 48, 48),    # 96 rows
+    (16, 16, 0, 6, 43, 48),   # 256 rows, the most a plan takes
+    (8, 8, 2, 2, 32, 32),     # 64 rows forced onto the tensor-core kernel
+    (16, 6, 1, 2, 48, None),  # CUDA-core kernel: 64 rows per block
+    (8, 8, 1, 1, 64, None),
+])
+def test_plan_row_blocks(B, q_len, hq, kernel, blocks, block_rows, threads_of):
+    plan = B.dflash_verify_attn_plan(problem(B, q_len=q_len, num_q_heads=hq, kernel=kernel))
+    R = q_len * hq
+    assert plan.rows == R and plan.row_blocks == blocks
+    assert math.ceil(R / blocks) == block_rows and (blocks - 1) * block_rows < R
+    if threads_of is not None:
+        assert plan.kernel == B.DFLASH_KERNEL_TCGEN05
+        ref = B.dflash_verify_attn_plan(problem(B, q_len=1, num_q_heads=threads_of))
+        assert plan.threads == ref.threads and plan.smem_bytes == ref.smem_bytes
+    else:
+        assert plan.kernel == B.DFLASH_KERNEL_SIMT
+    # one wave: every (split, row block) CTA of the single sequence and KV head fits the SMs
+    cap = math.ceil(262144 / plan.min_split_keys)
+    assert plan.num_splits == min(152 // blocks, cap)
+    # the workspace holds every row of every slot, however the rows are blocked
+    assert plan.workspace_bytes >= plan.ws_acc_offset + plan.num_splits * R * 256 * 4
+    assert plan.ws_acc_offset >= plan.ws_state_offset + plan.num_splits * R * 8
+
+
+def test_plan_row_blocks_fused(B):
+    pr = problem(B, q_len=16, batch=4)
+    pr.flags = B.DFLASH_PROBLEM_FUSED_COMBINE
+    plan = B.dflash_verify_attn_plan(pr)
+    assert plan.combine_fused == 1 and plan.row_blocks == 2
+    assert 4 * plan.row_blocks * plan.num_splits <= 152
+
+
+@pytest.mark.parametrize("row_blocks", [0, -1, 1, 97])
+def test_plan_row_blocks_tampered(B, row_blocks):
+    # a plan whose row blocks do not cover R in blocks the kernel can hold is refused
+    plan = B.dflash_verify_attn_plan(problem(B, q_len=16))
+    plan.row_blocks = row_blocks
+    lens = [262144]
+    with pytest.raises(B.DflashError) as e:
+        B.dflash_verify_attn_split_slots(plan, lens)
+    assert e.value.status == B.DFLASH_ERR_INVALID_ARGUMENT
 
 
 @pytest.mark.parametrize("n", [0, 1, 7, 8, 100, 1024, 32768, 131072, 261888, 262144, 300000])

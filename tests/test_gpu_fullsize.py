@@ -12,7 +12,8 @@ from speculative_verify_paged_e4m3_gb300 import workload as W
 pytestmark = pytest.mark.gpu
 
 CASES = [W.config1(), W.config2(), W.config3(), W.config5(), W.config6(4, 65536)] + [
-    W.config4(q, n) for n in W.TAIL_CONTEXTS for q in W.TAIL_QLENS]
+    W.config4(q, n) for n in W.TAIL_CONTEXTS for q in W.TAIL_QLENS] + [
+    W.config4(16, 262144), W.config4(10, 65536)]  # more rows than one CTA holds: row blocks
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -80,10 +80,32 @@ def test_batch_ragged_two_kv_heads(kernel):
     check(small("b3_hkv2", [1500, 17, 640], Hq=12, Hkv=2, seed=3), kernel)
 
 
-def test_sixty_four_rows_auto_kernel():
-    # 64 rows per KV head is above the tensor-core kernel's 48; the planner picks the CUDA-core one
-    att, *_ = check(small("g8_q8", [900], Hq=8, Hkv=1, seed=5), 0)
-    assert att.plan.kernel == 1
+@pytest.mark.parametrize("kernel", KERNELS + [0])
+@pytest.mark.parametrize("q_len,Hq,Hkv,ctx", [
+    (9, 6, 1, [1031]),          # 54 rows: two blocks of 27
+    (10, 6, 1, [300]),          # one split per block pair, ragged tail tile
+    (16, 6, 1, [4100]),         # 96 rows: two full blocks of 48 (CUDA-core: 48 as well)
+    (8, 8, 1, [900]),           # 64 rows
+    (16, 16, 1, [2000]),        # 256 rows, the most a plan takes
+    (11, 6, 1, [11]),           # context exactly q_len
+    (16, 12, 2, [1500, 17, 640]),  # ragged batch, two KV heads, 96 rows each
+])
+def test_row_blocks(kernel, q_len, Hq, Hkv, ctx):
+    # more rows per KV head than one CTA carries: each split's rows are dealt to row blocks
+    att, *_ = check(small(f"q{q_len}_g{Hq // Hkv}", ctx, q_len=q_len, Hq=Hq, Hkv=Hkv,
+                          seed=q_len * 13 + Hq), kernel)
+    R = q_len * Hq // Hkv
+    cap = 64 if att.plan.kernel == 1 else 48
+    assert att.plan.rows == R and att.plan.row_blocks == math.ceil(R / cap)
+    if kernel == 0:
+        assert att.plan.kernel == 2  # the tensor-core kernel whenever a block fits it
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("splits", [1, 3, 40])
+def test_row_blocks_forced_splits(kernel, splits):
+    check(small(f"q16_splits{splits}", [3000], q_len=16, seed=200 + splits), kernel,
+          num_splits=splits)
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
@@ -92,8 +114,9 @@ def test_peaked_softmax(kernel):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
-def test_workspace_state_matches_oracle_partials(kernel):
-    w = small("partials", [2500], seed=21)
+@pytest.mark.parametrize("q_len", [8, 16])
+def test_workspace_state_matches_oracle_partials(kernel, q_len):
+    w = small("partials", [2500], q_len=q_len, seed=21)
     att, inp, dev, out, lse = check(w, kernel, num_splits=5)
     from speculative_verify_paged_e4m3_gb300 import binding as B
     starts, active = B.dflash_verify_attn_split_bounds(att.plan, 2500)
@@ -214,14 +237,15 @@ def test_debug_dequant_bit_exact():
         assert np.array_equal(to_np(scd)[~nan].view(np.uint32), ref_scaled.view(np.uint32))
 
 
-def test_fused_and_separate_combine_agree_bitwise():
+@pytest.mark.parametrize("q_len", [8, 16])
+def test_fused_and_separate_combine_agree_bitwise(q_len):
     """The fused forward runs the same merge arithmetic as the combine kernel: same bits."""
     from speculative_verify_paged_e4m3_gb300 import binding as B
-    w = small("fused_vs_sep", [5000], seed=71)
+    w = small("fused_vs_sep", [5000], q_len=q_len, seed=71)
     dev = to_device(W.make_layer(w, 0, device="cpu"))
     res = []
     for flags in (B.DFLASH_PROBLEM_FUSED_COMBINE, 0):
-        att = B.VerifyAttention(1, 8, 6, 1, 256, 16, dev["block_table"].shape[1],
+        att = B.VerifyAttention(1, q_len, 6, 1, 256, 16, dev["block_table"].shape[1],
                                 dev["k_pool"].shape[0], 5000, num_splits=9,
                                 kernel=B.DFLASH_KERNEL_TCGEN05, flags=flags)
         assert att.plan.combine_fused == (1 if flags else 0)
