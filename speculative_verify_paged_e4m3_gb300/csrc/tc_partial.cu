@@ -232,13 +232,23 @@ __device__ __forceinline__ bool group_sync(const Ctx& ctx, int g, int wq, int& e
 
 // Source row in the page pool of the 16-key chunk starting at key j0 of sequence b: read from the
 // split's cache when the chunk is in it, else straight from the block table.
+// (pool row, clamped?) of key j0 of sequence b from the block table; out of line, as splits
+// longer than the row cache are rare
+__device__ __noinline__ int2 table_row(const int32_t* block_table, int b, int max_pages_per_seq,
+                                       int page_size, int num_pages, int j0) {
+    bool clamped = false;
+    const int phys = physical_page(block_table, b, max_pages_per_seq, j0 / page_size, num_pages,
+                                   &clamped);
+    return make_int2(phys * page_size + (j0 % page_size), clamped ? 1 : 0);
+}
+
 __device__ __forceinline__ int chunk_row(const PartialParams& p, const Small& sm, int b, int start,
                                          int j0, bool* clamped) {
     const int c = (j0 - start) / kChunk;
     if (c < kRowCache) return sm.rows[c];
-    const int phys = physical_page(p.block_table, b, p.max_pages_per_seq, j0 / p.page_size,
-                                   p.num_pages, clamped);
-    return phys * p.page_size + (j0 % p.page_size);
+    const int2 r = table_row(p.block_table, b, p.max_pages_per_seq, p.page_size, p.num_pages, j0);
+    if (r.y) *clamped = true;
+    return r.x;
 }
 
 // The three term slices (columns base, base + RP, base + 2RP) of this lane's 16 rows, combined
@@ -297,7 +307,7 @@ __device__ __forceinline__ bool grid_barrier(unsigned long long* ctr, uint32_t n
 // (each 256-thread half of the CTA has its own named barrier and scratch at the base of the
 // CTA's shared memory, unused by then).
 template <int NT>
-__device__ __forceinline__ void fused_merge(const PartialParams& p, uint8_t* smem) {
+__device__ __noinline__ void fused_merge(const PartialParams p, uint8_t* smem) {
     constexpr int kHalves = NT / kCombineThreads;
     constexpr int kQuarters = kHeadDim / (4 * kCombineCols);
     volatile int* barrier_ok = reinterpret_cast<volatile int*>(smem + kHalves * sizeof(CombineScratch));
@@ -521,21 +531,14 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                     // every lane acquires the stage's release before the zeroing stores below
                     if (!ctx.wait_warp(&sm.vfree[vs], ((tv / kVStages) & 1) ^ 1)) break;
                     if (lane == 0) {
-                        int rows[kChunks];
-                        int nval = 0;
-#pragma unroll
-                        for (int c = 0; c < kChunks; ++c) {
-                            const int j0 = h0 + kChunk * c;
-                            rows[c] = j0 < end ? chunk_row(p, sm, b, start, j0, &clamped) : -1;
-                            nval += rows[c] >= 0;
-                        }
+                        const int nval = (nkeys + kChunk - 1) / kChunk;  // chunks holding a key
                         const uint32_t bar = smem_u32(&sm.vtail);
                         mbar_arrive_expect_tx(bar, nval * kChunk * kHeadDim);
                         const uint32_t dst = smem_u32(vstage);
-#pragma unroll
-                        for (int c = 0; c < kChunks; ++c) {
-                            if (rows[c] < 0) continue;
-                            tma_load_4d(dst + c * kChunkBytes, &vmap, 0, 0, 2 * h, rows[c] / 8, bar,
+#pragma unroll 1
+                        for (int c = 0; c < nval; ++c) {
+                            const int row = chunk_row(p, sm, b, start, h0 + kChunk * c, &clamped);
+                            tma_load_4d(dst + c * kChunkBytes, &vmap, 0, 0, 2 * h, row / 8, bar,
                                         stream);
                         }
                     }
@@ -802,11 +805,13 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             if (lane == 0) mbar_arrive(smem_u32(&sm.sempty));  // S free for QK(t+1)
             uint32_t validm = rowmask;  // bit i: key j visible to row row0 + i
             if (!((tile0 + kTile <= end) && (tile0 + kTile - 1 <= qoff))) {
-#pragma unroll
-                for (int i = 0; i < kGroupRows; ++i) {
-                    const bool v = j < end && j <= qoff + (row_lo + row0 + i) / G;
-                    if (!v) validm &= ~(1u << i);
-                }
+                // row r of the slot (query token r / G) sees key j iff r / G >= j - qoff, that is
+                // r >= (j - qoff) G: the group's rows from `first` on
+                const int first = (j - qoff) * G - row_lo - row0;
+                if (j >= end)
+                    validm = 0;
+                else if (first > 0)
+                    validm &= first >= kGroupRows ? 0u : (0xFFFFFFFFu << first);
             }
             // e = y + (s - m): the exponent of the shifted probability; would any visible one
             // exceed 2^8?
