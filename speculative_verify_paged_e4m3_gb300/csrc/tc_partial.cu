@@ -307,7 +307,7 @@ __device__ __forceinline__ bool grid_barrier(unsigned long long* ctr, uint32_t n
 // (each 256-thread half of the CTA has its own named barrier and scratch at the base of the
 // CTA's shared memory, unused by then).
 template <int NT>
-__device__ __noinline__ void fused_merge(const PartialParams p, uint8_t* smem) {
+__device__ __forceinline__ void fused_merge(const PartialParams& p, uint8_t* smem) {
     constexpr int kHalves = NT / kCombineThreads;
     constexpr int kQuarters = kHeadDim / (4 * kCombineCols);
     volatile int* barrier_ok = reinterpret_cast<volatile int*>(smem + kHalves * sizeof(CombineScratch));
@@ -349,7 +349,9 @@ __device__ __noinline__ void fused_merge(const PartialParams p, uint8_t* smem) {
     }
 }
 
-template <int RP>
+// kFused: the instance that merges the splits after the grid barrier (p.out set); the other
+// carries no merge code at all.
+template <int RP, bool kFused>
 __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     tc_partial_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const PartialParams p) {
@@ -382,7 +384,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     const int per = b >= 0 ? keys_per_split(n, us.count, p.tile_keys, p.min_split_keys) : 1;
     const int start = split * per;
     if (b < 0 || start >= n) {  // idle slot: the combine never reads it
-        if (p.out) fused_merge<C::kThreads>(p, smem);
+        if constexpr (kFused) fused_merge<C::kThreads>(p, smem);
         return;
     }
     const bool guessed = b == (int)blockIdx.z && split == rblk.xs && per == per_max;
@@ -1001,7 +1003,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
-    if (p.out) fused_merge<C::kThreads>(p, smem);
+    if constexpr (kFused) fused_merge<C::kThreads>(p, smem);
 }
 
 }  // namespace tc
@@ -1046,11 +1048,11 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-template <int RP>
+template <int RP, bool kFused>
 static cudaError_t launch_rp(const CUtensorMap& kmap, const CUtensorMap& vmap,
                              const PartialParams& p, cudaStream_t stream) {
     constexpr uint32_t smem = tc::smem_bytes<RP>();
-    cudaError_t e = cudaFuncSetAttribute(tc::tc_partial_kernel<RP>,
+    cudaError_t e = cudaFuncSetAttribute(tc::tc_partial_kernel<RP, kFused>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -1065,7 +1067,7 @@ static cudaError_t launch_rp(const CUtensorMap& kmap, const CUtensorMap& vmap,
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, tc::tc_partial_kernel<RP>, kmap, vmap, p);
+    return cudaLaunchKernelEx(&cfg, tc::tc_partial_kernel<RP, kFused>, kmap, vmap, p);
 }
 
 cudaError_t launch_tc_partial(const PartialParams& p, cudaStream_t stream) {
@@ -1095,9 +1097,12 @@ cudaError_t launch_tc_partial(const PartialParams& p, cudaStream_t stream) {
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r1 != CUDA_SUCCESS || r2 != CUDA_SUCCESS) return cudaErrorInvalidValue;
     switch (rp) {
-        case 16: return launch_rp<16>(kmap, vmap, p, stream);
-        case 32: return launch_rp<32>(kmap, vmap, p, stream);
-        default: return launch_rp<48>(kmap, vmap, p, stream);
+        case 16: return p.out ? launch_rp<16, true>(kmap, vmap, p, stream)
+                              : launch_rp<16, false>(kmap, vmap, p, stream);
+        case 32: return p.out ? launch_rp<32, true>(kmap, vmap, p, stream)
+                              : launch_rp<32, false>(kmap, vmap, p, stream);
+        default: return p.out ? launch_rp<48, true>(kmap, vmap, p, stream)
+                              : launch_rp<48, false>(kmap, vmap, p, stream);
     }
 }
 
