@@ -50,30 +50,41 @@ __device__ __forceinline__ void combine_item(const CombineParams& p, int r, int 
     constexpr int kCols = kCombineThreads / SL;
     static_assert(SL <= kCombineSplitLanes && kCols * SL == kCombineThreads, "item shape");
     const int sl = tid / kCols, col = tid % kCols;
-    n = count > 0 ? n : 0;
-    const int per = n > 0 ? keys_per_split(n, count, p.tile_keys, p.min_split_keys) : 1;
-    const int active = n > 0 ? (n + per - 1) / per : 0;
     const int64_t base = first;
     const int R = p.rows;
     const float4* acc4 = reinterpret_cast<const float4*>(p.ws_acc);
+    // The first fold round's loads go out before the context length is used: they only need the
+    // unit's slots, so for a single sequence (slots fixed by the plan) they overlap the length's
+    // load. Splits at or past the active count are masked below (their slots are read, not used).
+    float2 st[kCombineFold];
+    float4 a[kCombineFold];
+    if (count > 0) {
+#pragma unroll
+        for (int k = 0; k < kCombineFold; ++k) {
+            const int s = min(sl + k * SL, count - 1);  // clamped into the unit's slots
+            st[k] = __ldcg(&p.ws_state[(base + s) * R + r]);
+            a[k] = __ldcg(&acc4[((base + s) * R + r) * (kHeadDim / 4) + quarter * kCols + col]);
+        }
+    }
+    n = count > 0 ? n : 0;
+    const int per = n > 0 ? keys_per_split(n, count, p.tile_keys, p.min_split_keys) : 1;
+    const int active = n > 0 ? (n + per - 1) / per : 0;
 
     float m = -INFINITY, L = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = sl; s0 < active; s0 += SL * kCombineFold) {
-        // all loads of kCombineFold splits first (one round trip), then the fold; an active split
-        // always has its numerator written (zero for a row it does not see)
-        float2 st[kCombineFold];
-        float4 a[kCombineFold];
+        if (s0 != sl) {
+            // later rounds (more than SL * kCombineFold active splits): all loads first again
 #pragma unroll
-        for (int k = 0; k < kCombineFold; ++k) {
-            // unconditional loads (index clamped into the allocation), masked afterwards
-            const int s = min(s0 + k * SL, active - 1);
-            st[k] = __ldcg(&p.ws_state[(base + s) * R + r]);
-            a[k] = __ldcg(&acc4[((base + s) * R + r) * (kHeadDim / 4) + quarter * kCols + col]);
+            for (int k = 0; k < kCombineFold; ++k) {
+                const int s = min(s0 + k * SL, active - 1);
+                st[k] = __ldcg(&p.ws_state[(base + s) * R + r]);
+                a[k] = __ldcg(&acc4[((base + s) * R + r) * (kHeadDim / 4) + quarter * kCols + col]);
+            }
         }
 #pragma unroll
         for (int k = 0; k < kCombineFold; ++k) {
-            if (s0 + k * SL >= active) {
+            if (s0 + k * SL >= active) {  // an inactive split (or a clamped duplicate): no weight
                 st[k] = make_float2(-INFINITY, 0.f);
                 a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
