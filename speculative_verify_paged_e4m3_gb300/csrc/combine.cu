@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_rows_kernel(CombinePa
 #pragma unroll
             for (int k = 0; k < kBatchLoads; ++k) {
                 if (s0 + k >= active) break;
-                const float w = st[k].x == -INFINITY ? 0.f : exp2f(st[k].x - M);
+                const float w = st[k].x == -INFINITY ? 0.f : merge_ex2(st[k].x - M);
                 t.x = fmaf(w, a[k].x, t.x);
                 t.y = fmaf(w, a[k].y, t.y);
                 t.z = fmaf(w, a[k].z, t.z);

@@ -30,6 +30,14 @@ struct CombineScratch {
     float2 ml[kCombineSplitLanes];            // (running max, running sum) of each split lane
 };
 
+// 2^x for the merge weights (x <= 0): the hardware approximation, relative error about 2^-22;
+// results below 2^-126 flush to zero (such a split's weight is below FP32 resolution anyway).
+__device__ __forceinline__ float merge_ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ void combine_sync(int bar_id) {
     asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(kCombineThreads) : "memory");
 }
@@ -89,8 +97,8 @@ __device__ __forceinline__ void combine_item(const CombineParams& p, int r, int 
                 a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
             const float mn = fmaxf(m, st[k].x);
-            const float cr = mn == -INFINITY ? 1.f : exp2f(m - mn);
-            const float cs = mn == -INFINITY ? 0.f : exp2f(st[k].x - mn);
+            const float cr = mn == -INFINITY ? 1.f : merge_ex2(m - mn);
+            const float cs = mn == -INFINITY ? 0.f : merge_ex2(st[k].x - mn);
             L = fmaf(cs, st[k].y, L * cr);
             o.x = fmaf(cs, a[k].x, o.x * cr);
             o.y = fmaf(cs, a[k].y, o.y * cr);
@@ -104,15 +112,15 @@ __device__ __forceinline__ void combine_item(const CombineParams& p, int r, int 
     combine_sync(bar_id);
     if (tid < kCols) {
         float M = -INFINITY;
-#pragma unroll
+#pragma unroll 4
         for (int k = 0; k < SL; ++k) M = fmaxf(M, sh.ml[k].x);
         float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
         float Lt = 0.f;
         if (M != -INFINITY) {
-#pragma unroll
+#pragma unroll 4
             for (int k = 0; k < SL; ++k) {
                 const float2 ml = sh.ml[k];
-                const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+                const float w = ml.x == -INFINITY ? 0.f : merge_ex2(ml.x - M);
                 const float4 q = sh.part[k * kCols + tid];
                 t.x = fmaf(w, q.x, t.x);
                 t.y = fmaf(w, q.y, t.y);
