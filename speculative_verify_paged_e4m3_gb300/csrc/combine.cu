@@ -93,10 +93,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_rows_kernel(CombinePa
                 Lt = fmaf(w, st[k].y, Lt);
             }
         }
-        t.x /= Lt;
-        t.y /= Lt;
-        t.z /= Lt;
-        t.w /= Lt;
+        const float inv = 1.f / Lt;
+        t.x *= inv;
+        t.y *= inv;
+        t.z *= inv;
+        t.w *= inv;
     }
     const int i = r / p.group, g = r % p.group;
     const int64_t orow = ((int64_t)b * p.q_len + i) * p.num_q_heads + h * p.group + g;

@@ -61,51 +61,47 @@ __device__ __forceinline__ void combine_item(const CombineParams& p, int r, int 
     const int64_t base = first;
     const int R = p.rows;
     const float4* acc4 = reinterpret_cast<const float4*>(p.ws_acc);
-    // The first fold round's loads go out before the context length is used: they only need the
-    // unit's slots, so for a single sequence (slots fixed by the plan) they overlap the length's
-    // load. Splits at or past the active count are masked below (their slots are read, not used).
-    float2 st[kCombineFold];
-    float4 a[kCombineFold];
-    if (count > 0) {
-#pragma unroll
-        for (int k = 0; k < kCombineFold; ++k) {
-            const int s = min(sl + k * SL, count - 1);  // clamped into the unit's slots
-            st[k] = __ldcg(&p.ws_state[(base + s) * R + r]);
-            a[k] = __ldcg(&acc4[((base + s) * R + r) * (kHeadDim / 4) + quarter * kCols + col]);
-        }
-    }
-    n = count > 0 ? n : 0;
-    const int per = n > 0 ? keys_per_split(n, count, p.tile_keys, p.min_split_keys) : 1;
-    const int active = n > 0 ? (n + per - 1) / per : 0;
-
+    // Each fold round loads kCombineFold splits of this lane at once (indices clamped into the
+    // unit's slots, so no load needs the context length): the first round's loads go out
+    // before the length is used, which for a single sequence (slots fixed by the plan) overlaps
+    // the length's load. Splits at or past the active count are masked in the fold (their slots
+    // are read, not used).
     float m = -INFINITY, L = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = sl; s0 < active; s0 += SL * kCombineFold) {
-        if (s0 != sl) {
-            // later rounds (more than SL * kCombineFold active splits): all loads first again
+    if (count > 0) {
+        int active = 0;
+        int s0 = sl;
+        do {
+            float2 st[kCombineFold];
+            float4 a[kCombineFold];
 #pragma unroll
             for (int k = 0; k < kCombineFold; ++k) {
-                const int s = min(s0 + k * SL, active - 1);
+                const int s = min(s0 + k * SL, count - 1);
                 st[k] = __ldcg(&p.ws_state[(base + s) * R + r]);
                 a[k] = __ldcg(&acc4[((base + s) * R + r) * (kHeadDim / 4) + quarter * kCols + col]);
             }
-        }
-#pragma unroll
-        for (int k = 0; k < kCombineFold; ++k) {
-            if (s0 + k * SL >= active) {  // an inactive split (or a clamped duplicate): no weight
-                st[k] = make_float2(-INFINITY, 0.f);
-                a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (s0 == sl) {
+                const int per = n > 0 ? keys_per_split(n, count, p.tile_keys, p.min_split_keys) : 1;
+                active = n > 0 ? (n + per - 1) / per : 0;
             }
-            const float mn = fmaxf(m, st[k].x);
-            const float cr = mn == -INFINITY ? 1.f : merge_ex2(m - mn);
-            const float cs = mn == -INFINITY ? 0.f : merge_ex2(st[k].x - mn);
-            L = fmaf(cs, st[k].y, L * cr);
-            o.x = fmaf(cs, a[k].x, o.x * cr);
-            o.y = fmaf(cs, a[k].y, o.y * cr);
-            o.z = fmaf(cs, a[k].z, o.z * cr);
-            o.w = fmaf(cs, a[k].w, o.w * cr);
-            m = mn;
-        }
+#pragma unroll
+            for (int k = 0; k < kCombineFold; ++k) {
+                if (s0 + k * SL >= active) {  // inactive split or clamped duplicate: no weight
+                    st[k] = make_float2(-INFINITY, 0.f);
+                    a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                const float mn = fmaxf(m, st[k].x);
+                const float cr = mn == -INFINITY ? 1.f : merge_ex2(m - mn);
+                const float cs = mn == -INFINITY ? 0.f : merge_ex2(st[k].x - mn);
+                L = fmaf(cs, st[k].y, L * cr);
+                o.x = fmaf(cs, a[k].x, o.x * cr);
+                o.y = fmaf(cs, a[k].y, o.y * cr);
+                o.z = fmaf(cs, a[k].z, o.z * cr);
+                o.w = fmaf(cs, a[k].w, o.w * cr);
+                m = mn;
+            }
+            s0 += SL * kCombineFold;
+        } while (s0 < active);
     }
     sh.part[sl * kCols + col] = o;
     if (col == 0) sh.ml[sl] = make_float2(m, L);
@@ -128,10 +124,11 @@ __device__ __forceinline__ void combine_item(const CombineParams& p, int r, int 
                 t.w = fmaf(w, q.w, t.w);
                 Lt = fmaf(w, ml.y, Lt);
             }
-            t.x /= Lt;
-            t.y /= Lt;
-            t.z /= Lt;
-            t.w /= Lt;
+            const float inv = 1.f / Lt;
+            t.x *= inv;
+            t.y *= inv;
+            t.z *= inv;
+            t.w *= inv;
         }
         const int i = r / p.group, g = r % p.group;
         const int64_t orow = ((int64_t)b * p.q_len + i) * p.num_q_heads + h * p.group + g;
