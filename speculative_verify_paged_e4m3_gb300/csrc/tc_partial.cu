@@ -230,8 +230,6 @@ __device__ __forceinline__ bool group_sync(const Ctx& ctx, int g, int wq, int& e
     return group_wait(ctx, g, group_arrive(ctx, g, wq, epoch, vote), any);
 }
 
-// Source row in the page pool of the 16-key chunk starting at key j0 of sequence b: read from the
-// split's cache when the chunk is in it, else straight from the block table.
 // (pool row, clamped?) of key j0 of sequence b from the block table; out of line, as splits
 // longer than the row cache are rare
 __device__ __noinline__ int2 table_row(const int32_t* block_table, int b, int max_pages_per_seq,
@@ -242,6 +240,8 @@ __device__ __noinline__ int2 table_row(const int32_t* block_table, int b, int ma
     return make_int2(phys * page_size + (j0 % page_size), clamped ? 1 : 0);
 }
 
+// Source row in the page pool of the 16-key chunk starting at key j0 of sequence b: read from the
+// split's cache when the chunk is in it, else straight from the block table.
 __device__ __forceinline__ int chunk_row(const PartialParams& p, const Small& sm, int b, int start,
                                          int j0, bool* clamped) {
     const int c = (j0 - start) / kChunk;
