@@ -142,15 +142,15 @@ int dflash_verify_attn_plan(const dflash_verify_attn_problem* problem,
 /*
  * Split slots (host restatement of the device rule). The workspace holds slots = batch * Hkv *
  * num_splits split states, one per partial-kernel CTA. They are shared out among the
- * (sequence, KV head) units u = b * Hkv + h by context length, counted in 128-key granules
- * g_u = ceil(n_b / 128) (n_b = context_lens[b] clamped to [0, max_context]): each non-empty
- * unit owns one slot, and the other slots - E go in proportion to x_u = max(slots * g_u - G, 0),
- * the unit's length beyond one even share:
- *   slot_start[u] = (non-empty units before u) + floor((slots - E) * (x of the units before u) / X)
- * (E non-empty units, G = sum of g, X = sum of x; when X is 0 the slots past E stay idle). Every
- * non-empty unit owns at least one slot, an empty unit none, units at least one even share long
- * get splits of about G / slots granules; with equal lengths every unit owns num_splits slots
- * (the [batch, Hkv, num_splits, R] layout). Unit u splits its n_b keys into pieces of
+ * (sequence, KV head) units u = b * Hkv + h so that the busiest slot holds as few 128-key tiles
+ * as possible. With w_b = ceil(n_b / 128) tiles in sequence b (n_b = context_lens[b] clamped to
+ * [0, max_context]), T is the smallest tile count with
+ *   Hkv * sum_b ceil(w_b / T) <= slots,
+ * and each KV head of sequence b owns c_b = ceil(w_b / T) contiguous slots:
+ *   slot_start[b * Hkv + h] = Hkv * (c of the sequences before b) + h * c_b.
+ * Slots past slot_start[batch * Hkv] stay idle. A single sequence (batch 1) keeps num_splits
+ * slots per KV head. Every non-empty unit owns at least one slot, an empty unit none. Unit u
+ * splits its n_b keys into pieces of
  * keys_per_split[u] = roundup(max(ceil(n_b / S_u), min_split_keys), tile_keys) keys, S_u =
  * slot_start[u + 1] - slot_start[u]; its first active[u] = ceil(n_b / keys_per_split[u]) slots
  * hold state (0 for an empty unit). context_lens: batch entries (host memory); slot_start:

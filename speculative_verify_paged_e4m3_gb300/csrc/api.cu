@@ -217,37 +217,44 @@ int dflash_verify_attn_split_slots(const dflash_verify_attn_plan_t* plan,
         return DFLASH_ERR_INVALID_ARGUMENT;
     const dflash_verify_attn_problem& pr = plan->problem;
     const int B = pr.batch, Hkv = pr.num_kv_heads;
-    std::vector<int64_t> n(B), g(B);
-    int64_t G = 0, E = 0;
+    const int64_t S = plan->num_splits;
+    std::vector<int64_t> n(B), w(B);
+    int64_t W = 0, wmax = 0;
     for (int b = 0; b < B; ++b) {
         int64_t nb = context_lens[b];
         nb = nb > pr.max_context ? pr.max_context : nb;
         nb = nb < 0 ? 0 : nb;
         n[b] = nb;
-        g[b] = (nb + 127) / 128;
-        G += g[b] * Hkv;
-        E += g[b] > 0 ? Hkv : 0;
+        w[b] = (nb + 127) / 128;
+        W += w[b];
+        wmax = w[b] > wmax ? w[b] : wmax;
     }
-    const int64_t slots = (int64_t)B * Hkv * plan->num_splits;
-    // one slot per non-empty unit, the rest in proportion to each unit's length beyond one even
-    // share G / slots (common.cuh, locate_slots)
-    std::vector<int64_t> x(B);
-    int64_t X = 0;
-    for (int b = 0; b < B; ++b) {
-        x[b] = g[b] > 0 && slots * g[b] > G ? slots * g[b] - G : 0;
-        X += x[b] * Hkv;
-    }
-    int64_t x_before = 0, e_before = 0;
-    for (int b = 0; b < B; ++b) {
-        for (int h = 0; h < Hkv; ++h) {
-            const int u = b * Hkv + h;
-            slot_start[u] =
-                G == 0 ? 0 : (int32_t)(e_before + (X > 0 ? (slots - E) * x_before / X : 0));
-            x_before += x[b];
-            e_before += g[b] > 0 ? 1 : 0;
+    // slots per KV head of each sequence (common.cuh, locate_slots): num_splits for a single
+    // sequence; for a batch c_b = ceil(w_b / T), T the smallest tile count per split with
+    // Hkv * sum_b ceil(w_b / T) <= slots
+    std::vector<int64_t> c(B, 0);
+    if (W > 0 && B == 1) {
+        c[0] = S;
+    } else if (W > 0) {
+        const int64_t C = (int64_t)B * Hkv * S;
+        int64_t lo = 1, hi = wmax;  // T = wmax leaves one slot per non-empty unit: Hkv E <= C
+        while (lo < hi) {
+            const int64_t mid = (lo + hi) / 2;
+            int64_t need = 0;
+            for (int b = 0; b < B; ++b) need += ceil_div(w[b], mid);
+            if (need * Hkv <= C)
+                hi = mid;
+            else
+                lo = mid + 1;
         }
+        for (int b = 0; b < B; ++b) c[b] = ceil_div(w[b], lo);
     }
-    slot_start[B * Hkv] = G == 0 ? 0 : (int32_t)(E + (X > 0 ? slots - E : 0));
+    int64_t before = 0;
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < Hkv; ++h) slot_start[b * Hkv + h] = (int32_t)(Hkv * before + h * c[b]);
+        before += c[b];
+    }
+    slot_start[B * Hkv] = (int32_t)(Hkv * before);
     for (int b = 0; b < B; ++b) {
         for (int h = 0; h < Hkv; ++h) {
             const int u = b * Hkv + h;

@@ -114,16 +114,16 @@ __device__ __forceinline__ int physical_page(const int32_t* block_table, int b,
 }
 
 // ---- split slots of a batch -------------------------------------------------------------------
-// The plan's batch * Hkv * S split slots (one CTA each) are shared out among the (sequence, KV
-// head) units by context length, counted in 128-key granules w_u: every non-empty unit owns one
-// slot, and the other C - E slots (C slots, E non-empty units) go in proportion to each unit's
-// length beyond one even share W / C (W granules in all), x_u = max(C w_u - W, 0). Unit
-// u = b * Hkv + h owns the contiguous slots [start(u), start(u + 1)) with
-//   start(u) = (non-empty units before u) + floor((C - E) * (x of the units before u) / X)
-// (X = sum of x; when X is 0 every non-empty unit owns one slot and the rest stay idle). A unit
-// at least one even share long then gets splits of about W / C granules, the same for all; an
-// empty unit owns no slot; units of equal length own S slots each (the [batch, Hkv, S] layout).
-// dflash_verify_attn_split_slots does the same integer arithmetic on the host.
+// The plan's C = batch * Hkv * S split slots (one CTA each) are shared out among the (sequence,
+// KV head) units so that the busiest slot has as few 128-key tiles as possible. With w_b =
+// ceil(n_b / 128) tiles in sequence b, T is the smallest tile count with
+//   Hkv * sum_b ceil(w_b / T) <= C,
+// and each KV head of sequence b owns c_b = ceil(w_b / T) contiguous slots, unit u = b * Hkv + h
+// from slot Hkv * (c of the sequences before b) + h * c_b; the slots past all units stay idle.
+// A unit's splits then hold at most T tiles each (the least any split of the units into
+// contiguous pieces achieves), an empty unit owns no slot. A single sequence keeps num_splits
+// slots per KV head (the same splits: its units are equal). dflash_verify_attn_split_slots does
+// the same integer arithmetic on the host.
 struct UnitSlots {
     int b, h;    // the unit (b = -1: no unit owns the slot)
     int first;   // its first slot
@@ -174,90 +174,77 @@ __device__ __forceinline__ UnitSlots locate_slots_batch_body(const int32_t* cont
                                                              int key, bool by_slot) {
     const int lane = threadIdx.x & 31;
     UnitSlots r = {-1, 0, 0, 0, 0, 0};
-    auto length = [&](int b, int* flags) {
-        return slot_length(context_lens, b, max_context, q_len, flags);
+    int unused = 0;
+    auto tiles = [&](int b) {  // w_b (0 past the batch)
+        return b < B ? slot_granules(slot_length(context_lens, b, max_context, q_len, &unused)) : 0;
     };
-    // totals over the batch (per sequence; every KV head of a sequence has its weight)
+    // tiles in all (W), the longest sequence, non-empty sequences, the batch's context flags
     long long W = 0;
-    int E = 0, flags = 0;
+    int wmax = 0, E = 0, flags = 0;
     for (int b0 = 0; b0 < B; b0 += 32) {
-        const int w = b0 + lane < B ? slot_granules(length(b0 + lane, &flags)) : 0;
+        const int b = b0 + lane;
+        const int w = b < B ? slot_granules(slot_length(context_lens, b, max_context, q_len, &flags))
+                            : 0;
         W += w;
+        wmax = max(wmax, w);
         E += w > 0;
     }
     for (int o = 16; o > 0; o >>= 1) {
         W += __shfl_xor_sync(0xffffffffu, W, o);
+        wmax = max(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
         E += __shfl_xor_sync(0xffffffffu, E, o);
         flags |= __shfl_xor_sync(0xffffffffu, flags, o);
     }
     r.flags = flags;
     if (W == 0) return r;
-    W *= Hkv;
-    E *= Hkv;
-    const long long C = (long long)B * Hkv * S;
-    const long long rest = C - E;
-    auto excess = [&](int w) { return w > 0 && C * w > W ? C * w - W : 0ll; };
-    long long X = 0;
-    for (int b0 = 0; b0 < B; b0 += 32) {
-        int unused = 0;
-        X += b0 + lane < B ? excess(slot_granules(length(b0 + lane, &unused))) : 0;
+    // T: binary search between W Hkv / C (no split can do better) and the first count that is
+    // surely enough, W Hkv / (C - U) (U = Hkv E: each unit's last split may be short), or wmax
+    const long long C = (long long)B * Hkv * S, U = (long long)Hkv * E;
+    long long lo = (W * Hkv + C - 1) / C;
+    long long hi = wmax;
+    if (C > U) hi = min(hi, (W * Hkv + (C - U) - 1) / (C - U));
+    lo = max(1ll, min(lo, hi));
+    while (lo < hi) {
+        const long long mid = (lo + hi) >> 1;
+        long long need = 0;
+        for (int b0 = 0; b0 < B; b0 += 32) need += (tiles(b0 + lane) + mid - 1) / mid;
+        for (int o = 16; o > 0; o >>= 1) need += __shfl_xor_sync(0xffffffffu, need, o);
+        if (need * Hkv <= C)
+            hi = mid;
+        else
+            lo = mid + 1;
     }
-    for (int o = 16; o > 0; o >>= 1) X += __shfl_xor_sync(0xffffffffu, X, o);
-    X *= Hkv;
-    long long x_carry = 0;
-    int e_carry = 0;
+    const int T = (int)lo;
+    // slots per KV head of each sequence, scanned over the batch
+    int c_carry = 0;
     for (int b0 = 0; b0 < B; b0 += 32) {
         const int b = b0 + lane;
-        int unused = 0;
-        const int n = b < B ? length(b, &unused) : 0;
-        const int w = slot_granules(n);
-        const long long x = excess(w);
-        long long sw = x;  // inclusive scans over the chunk
-        int se = w > 0;
+        const int n = b < B ? slot_length(context_lens, b, max_context, q_len, &unused) : 0;
+        const int c = (slot_granules(n) + T - 1) / T;
+        int sc = c;  // inclusive scan over the chunk
         for (int o = 1; o < 32; o <<= 1) {
-            const long long tw = __shfl_up_sync(0xffffffffu, sw, o);
-            const int te = __shfl_up_sync(0xffffffffu, se, o);
-            if (lane >= o) {
-                sw += tw;
-                se += te;
-            }
+            const int t = __shfl_up_sync(0xffffffffu, sc, o);
+            if (lane >= o) sc += t;
         }
-        const long long x_before = x_carry + sw - x;  // excess of the sequences before b
-        const int e_before = e_carry + se - (w > 0);   // non-empty sequences before b
-        // slot h of sequence b (excess xb per KV head) starts at
-        auto start = [&](long long xb0, int eb0, bool nonempty, long long xb, int hh) {
-            return (long long)Hkv * eb0 + (nonempty ? hh : 0) +
-                   (X > 0 ? rest * ((long long)Hkv * xb0 + (long long)hh * xb) / X : 0);
-        };
-        bool mine;
-        if (by_slot)
-            mine = b < B && w > 0 && key >= start(x_before, e_before, true, x, 0) &&
-                   key < start(x_before, e_before, true, x, Hkv);
-        else
-            mine = b == key / Hkv;
+        const int c_before = c_carry + sc - c;  // per KV head, sequences before b
+        const bool mine = by_slot ? (b < B && c > 0 && key >= Hkv * c_before &&
+                                     key < Hkv * (c_before + c))
+                                  : b == key / Hkv;
         const unsigned m = __ballot_sync(0xffffffffu, mine);
         if (m) {
             const int src = __ffs(m) - 1;
-            const long long xb0 = __shfl_sync(0xffffffffu, x_before, src);
-            const int eb0 = __shfl_sync(0xffffffffu, e_before, src);
-            const long long xb = __shfl_sync(0xffffffffu, x, src);
+            const int cb0 = __shfl_sync(0xffffffffu, c_before, src);
+            const int cb = __shfl_sync(0xffffffffu, c, src);
             const int nb = __shfl_sync(0xffffffffu, n, src);
-            const bool nonempty = nb > 0;
-            int hh = 0;
-            if (by_slot) {
-                while (hh + 1 < Hkv && start(xb0, eb0, nonempty, xb, hh + 1) <= key) ++hh;
-            } else {
-                hh = key % Hkv;
-            }
+            const int hh = by_slot ? (key - Hkv * cb0) / cb : key % Hkv;
             r.b = b0 + src;
             r.h = hh;
-            r.first = (int)start(xb0, eb0, nonempty, xb, hh);
-            r.count = (int)(start(xb0, eb0, nonempty, xb, hh + 1) - r.first);
+            r.first = Hkv * cb0 + hh * cb;
+            r.count = cb;
             r.n = nb;
             return r;
         }
-        x_carry += __shfl_sync(0xffffffffu, sw, 31);
-        e_carry += __shfl_sync(0xffffffffu, se, 31);
+        c_carry += __shfl_sync(0xffffffffu, sc, 31);
     }
     return r;
 }

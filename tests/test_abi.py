@@ -269,9 +269,9 @@ def test_default_split_count_fills_one_wave(B):
 
 
 def test_split_slots_layout(B):
-    """Slots go to (sequence, KV head) units in proportion to length: equal lengths give
-    num_splits slots each (the [batch, Hkv, S] layout), every non-empty unit gets at least one,
-    an empty unit none, and they add up to batch * Hkv * num_splits."""
+    """Slots go to (sequence, KV head) units so that the busiest split is as short as possible:
+    equal lengths here give num_splits slots each (the [batch, Hkv, S] layout), every non-empty
+    unit gets at least one, an empty unit none, and they fit in batch * Hkv * num_splits."""
     plan = B.dflash_verify_attn_plan(problem(B, batch=4, num_q_heads=24, num_kv_heads=4,
                                              max_pages_per_seq=4096, num_pages=20000,
                                              max_context=65536))
@@ -283,7 +283,7 @@ def test_split_slots_layout(B):
     lens = [65536, 57344, 0, 40960]
     start, per, act = B.dflash_verify_attn_split_slots(plan, lens)
     cnt = [start[u + 1] - start[u] for u in range(units)]
-    assert start[0] == 0 and start[-1] == units * S and all(c >= 0 for c in cnt)
+    assert start[0] == 0 and start[-1] <= units * S and all(c >= 0 for c in cnt)
     for u in range(units):
         n = lens[u // 4]
         assert (cnt[u] == 0) == (n == 0) and (act[u] == 0) == (n == 0)
@@ -294,6 +294,30 @@ def test_split_slots_layout(B):
     for u in range(units):
         if lens[u // 4]:
             assert abs(share[u] - lens[u // 4] / total) * units * S <= 1.5
-    # the longest sequence's splits are no longer than about the average
+    # the longest split is no longer than about the average
     tiles = [math.ceil(p / 128) for p, a in zip(per, act) if a]
     assert max(tiles) <= math.ceil(sum(math.ceil(n / 128) for n in lens) * 4 / (units * S)) + 2
+
+
+@pytest.mark.parametrize("lens", [
+    [65536, 57344, 49152, 40960],      # the ragged whole-model-heads workload
+    [262144, 1000, 300000, 77, 0, 5000, 131072, 4096],
+    [128] * 3 + [262144],
+    [1, 2, 3],
+])
+def test_split_slots_min_max_rule(B, lens):
+    """The busiest slot holds the fewest tiles any split into contiguous, equal pieces per unit
+    can give: brute force over T against the host rule."""
+    Hkv = 4
+    plan = B.dflash_verify_attn_plan(problem(B, batch=len(lens), num_q_heads=24, num_kv_heads=Hkv,
+                                             max_pages_per_seq=16384, num_pages=20000))
+    C = len(lens) * Hkv * plan.num_splits
+    w = [math.ceil(min(max(n, 0), 262144) / 128) for n in lens]
+    T = next(t for t in range(1, max(w) + 1)
+             if Hkv * sum(math.ceil(x / t) for x in w) <= C)
+    start, per, act = B.dflash_verify_attn_split_slots(plan, lens)
+    cnt = [start[u + 1] - start[u] for u in range(len(lens) * Hkv)]
+    assert cnt == [math.ceil(x / T) for x in w for _ in range(Hkv)]
+    assert start[-1] <= C
+    tiles = [math.ceil(p / 128) for p, a in zip(per, act) if a]
+    assert max(tiles) <= max(T, plan.min_split_keys // 128)
