@@ -66,7 +66,7 @@
 extern "C" {
 #endif
 
-#define DFLASH_VERIFY_ATTN_VERSION 2
+#define DFLASH_VERIFY_ATTN_VERSION 3
 
 typedef enum {
     DFLASH_OK = 0,
@@ -123,6 +123,11 @@ typedef struct {
     int32_t row_blocks;       /* CTAs per split, each carrying ceil(R / row_blocks) consecutive
                                  rows (1 unless R exceeds what one CTA of the kernel holds: 48
                                  rows for TCGEN05, 64 for SIMT) */
+    int32_t num_slots;        /* split slots of the workspace, one partial-kernel CTA (per row
+                                 block) each: batch * Hkv * num_splits for a single sequence or a
+                                 forced split count; for a batch on the planner's split count, the
+                                 SMs' worth (sm_count / row_blocks, at least batch * Hkv), shared
+                                 out by length at run time (dflash_verify_attn_split_slots) */
     size_t workspace_bytes;   /* caller allocates at least this many bytes */
     size_t ws_state_offset;   /* float2 (m, l) [slots, R]; m in log2 units (slots below) */
     size_t ws_acc_offset;     /* float numerator [slots, R, head_dim], v_scale applied */
@@ -140,8 +145,8 @@ int dflash_verify_attn_plan(const dflash_verify_attn_problem* problem,
                             dflash_verify_attn_plan_t* plan);
 
 /*
- * Split slots (host restatement of the device rule). The workspace holds slots = batch * Hkv *
- * num_splits split states, one per partial-kernel CTA. They are shared out among the
+ * Split slots (host restatement of the device rule). The workspace holds slots = num_slots split
+ * states, one per partial-kernel CTA (and row block). They are shared out among the
  * (sequence, KV head) units u = b * Hkv + h so that the busiest slot holds as few 128-key tiles
  * as possible. With w_b = ceil(n_b / 128) tiles in sequence b (n_b = context_lens[b] clamped to
  * [0, max_context]), T is the smallest tile count with

@@ -15,7 +15,7 @@ import torch
 
 from . import build as _build
 
-DFLASH_VERIFY_ATTN_VERSION = 2
+DFLASH_VERIFY_ATTN_VERSION = 3
 DFLASH_OK = 0
 DFLASH_ERR_INVALID_ARGUMENT = -1
 DFLASH_ERR_UNSUPPORTED = -2
@@ -54,7 +54,7 @@ class Problem(ctypes.Structure):
 class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "version", "kernel", "num_splits", "tile_keys", "min_split_keys", "rows", "threads",
-        "smem_bytes", "sm_count", "combine_fused", "row_blocks")] + [
+        "smem_bytes", "sm_count", "combine_fused", "row_blocks", "num_slots")] + [
         ("workspace_bytes", ctypes.c_size_t),
         ("ws_state_offset", ctypes.c_size_t),
         ("ws_acc_offset", ctypes.c_size_t),
@@ -280,11 +280,12 @@ class VerifyAttention:
         self.workspace = workspace
 
     def workspace_views(self):
-        """(status int32[1], state float32 [B,Hkv,S,R,2], acc float32 [B,Hkv,S,R,D]) views."""
+        """(status int32[1], state float32 [slots,R,2], acc float32 [slots,R,D]) views; for a
+        single sequence slot h * num_splits + s is split s of KV head h."""
         pr, pl = self.problem, self.plan
-        shape = (pr.batch, pr.num_kv_heads, pl.num_splits, pl.rows)
+        shape = (pl.num_slots, pl.rows)
         ws = self.workspace
-        n_state = pr.batch * pr.num_kv_heads * pl.num_splits * pl.rows * 2
+        n_state = pl.num_slots * pl.rows * 2
         state = ws[pl.ws_state_offset:pl.ws_state_offset + 4 * n_state].view(torch.float32)
         n_acc = n_state // 2 * pr.head_dim
         acc = ws[pl.ws_acc_offset:pl.ws_acc_offset + 4 * n_acc].view(torch.float32)

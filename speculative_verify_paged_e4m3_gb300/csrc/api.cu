@@ -58,6 +58,13 @@ int check_plan(const dflash_verify_attn_plan_t* plan) {
     if (plan->num_splits < 1 || plan->tile_keys < 1 || plan->rows < 1 || plan->row_blocks < 1 ||
         plan->row_blocks > plan->rows)
         return DFLASH_ERR_INVALID_ARGUMENT;
+    // slots: Hkv * num_splits for a single sequence (the grid (S, Hkv, 1)); at least one per
+    // unit for a batch
+    const int64_t units = (int64_t)plan->problem.batch * plan->problem.num_kv_heads;
+    if (plan->problem.batch < 1 || plan->problem.num_kv_heads < 1) return DFLASH_ERR_INVALID_ARGUMENT;
+    if (plan->problem.batch == 1 ? plan->num_slots != units * plan->num_splits
+                                 : plan->num_slots < units)
+        return DFLASH_ERR_INVALID_ARGUMENT;
     // every row block holds 1..capacity rows of the plan's kernel
     const int64_t block_rows = ceil_div(plan->rows, plan->row_blocks);
     const int capacity = plan->kernel == DFLASH_KERNEL_TCGEN05 ? tc_max_rows() : simt_max_rows();
@@ -96,6 +103,7 @@ PartialParams partial_params(const dflash_verify_attn_plan_t* plan, const void* 
     p.num_pages = pr.num_pages;
     p.max_context = pr.max_context;
     p.num_splits = plan->num_splits;
+    p.num_slots = plan->num_slots;
     p.tile_keys = plan->tile_keys;
     p.min_split_keys = plan->min_split_keys;
     p.grid_bar = reinterpret_cast<unsigned long long*>(ws + kGridBarrierOffset);
@@ -194,13 +202,26 @@ int dflash_verify_attn_plan(const dflash_verify_attn_problem* pr,
     }
     if (S < 1) S = 1;
     if (S > 65535) return DFLASH_ERR_UNSUPPORTED;
+    // Workspace slots. A single sequence, or a forced split count: units * S, the grid
+    // (S, Hkv, batch). A batch on the planner's split count: every SM's worth of slots (over the
+    // row blocks), shared out among the units by length at run time, so that units * S rounding
+    // leaves no SM idle.
+    int64_t slots = units * S;
+    if (pr->batch > 1 && pr->num_splits == 0) {
+        int64_t all = sm_count / row_blocks;
+        const int64_t cap = units * ceil_div(pr->max_context, plan->min_split_keys);
+        if (all > cap) all = cap;
+        if (all > slots) slots = all;
+    }
+    if (slots * row_blocks > 0x7FFFFFFF) return DFLASH_ERR_UNSUPPORTED;
     plan->num_splits = (int32_t)S;
+    plan->num_slots = (int32_t)slots;
     plan->combine_fused = fuse ? 1 : 0;
     plan->rows = (int32_t)rows;
     plan->row_blocks = row_blocks;
     plan->sm_count = sm_count;
-    const size_t state_bytes = (size_t)units * S * rows * sizeof(float2);
-    const size_t acc_bytes = (size_t)units * S * rows * kHeadDim * sizeof(float);
+    const size_t state_bytes = (size_t)slots * rows * sizeof(float2);
+    const size_t acc_bytes = (size_t)slots * rows * kHeadDim * sizeof(float);
     plan->ws_state_offset = kHeaderBytes;
     plan->ws_acc_offset = kHeaderBytes + align_up(state_bytes, 256);
     plan->workspace_bytes = plan->ws_acc_offset + acc_bytes;
@@ -231,12 +252,12 @@ int dflash_verify_attn_split_slots(const dflash_verify_attn_plan_t* plan,
     }
     // slots per KV head of each sequence (common.cuh, locate_slots): num_splits for a single
     // sequence; for a batch c_b = ceil(w_b / T), T the smallest tile count per split with
-    // Hkv * sum_b ceil(w_b / T) <= slots
+    // Hkv * sum_b ceil(w_b / T) <= num_slots
     std::vector<int64_t> c(B, 0);
     if (W > 0 && B == 1) {
         c[0] = S;
     } else if (W > 0) {
-        const int64_t C = (int64_t)B * Hkv * S;
+        const int64_t C = plan->num_slots;
         int64_t lo = 1, hi = wmax;  // T = wmax leaves one slot per non-empty unit: Hkv E <= C
         while (lo < hi) {
             const int64_t mid = (lo + hi) / 2;
@@ -370,6 +391,7 @@ int dflash_verify_attn_combine(const dflash_verify_attn_plan_t* plan, const void
     c.rows = plan->rows;
     c.max_context = pr.max_context;
     c.num_splits = plan->num_splits;
+    c.num_slots = plan->num_slots;
     c.tile_keys = plan->tile_keys;
     c.min_split_keys = plan->min_split_keys;
     if (launch_combine(c, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) {

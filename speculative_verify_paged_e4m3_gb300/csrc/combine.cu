@@ -20,7 +20,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_lanes_kernel(CombineP
     int first, count, n;
     if constexpr (kBatch) {  // several sequences: the unit's slots follow from every length
         const UnitSlots us = locate_slots(p.context_lens, p.batch, p.num_kv_heads, p.num_splits,
-                                          p.max_context, p.q_len, unit, false);
+                                          p.num_slots, p.max_context, p.q_len, unit, false);
         first = us.first;
         count = us.count;
         n = us.n;
@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_rows_kernel(CombinePa
     int first, count, n;
     if constexpr (kBatch) {
         const UnitSlots us = locate_slots(p.context_lens, p.batch, p.num_kv_heads, p.num_splits,
-                                          p.max_context, p.q_len, unit, false);
+                                          p.num_slots, p.max_context, p.q_len, unit, false);
         first = us.first;
         count = us.count;
         n = us.count > 0 ? us.n : 0;

@@ -27,6 +27,7 @@ struct PartialParams {
     int batch, q_len, num_q_heads, num_kv_heads, group, rows;
     int page_size, max_pages_per_seq, num_pages, max_context;
     int num_splits, tile_keys, min_split_keys;
+    int num_slots;  // workspace split slots: Hkv * num_splits for one sequence, else the plan's
     // Row blocks: the grid's x extent is num_splits * row_blocks; CTA x = split * row_blocks + k
     // carries rows [k * block_rows, min(rows, (k + 1) * block_rows)) of that split's slot.
     int row_blocks, block_rows;
@@ -45,10 +46,12 @@ struct CombineParams {
     float* lse;
     int batch, q_len, num_q_heads, num_kv_heads, group, rows;
     int max_context, num_splits, tile_keys, min_split_keys;
+    int num_slots;
 };
 
 // This CTA's place in a row-blocked grid: the split position x / row_blocks (the workspace slot
-// is that position plus num_splits per (KV head, sequence) grid row) and its row range.
+// is that position plus one grid row's worth per (y, z) grid row: a single sequence launches
+// (num_splits, Hkv, 1) slots, a batch (num_slots, 1, 1)) and its row range.
 struct RowBlock {
     int xs;      // split position within the grid row
     int slot;    // workspace slot
@@ -69,7 +72,7 @@ __device__ __forceinline__ RowBlock row_block(const PartialParams& p) {
     rb.xs = blockIdx.x / p.row_blocks;
     rb.row_lo = (blockIdx.x - rb.xs * p.row_blocks) * p.block_rows;
     rb.rows = min(p.block_rows, p.rows - rb.row_lo);
-    rb.slot = rb.xs + p.num_splits * (blockIdx.y + gridDim.y * blockIdx.z);
+    rb.slot = rb.xs + (gridDim.x / p.row_blocks) * (blockIdx.y + gridDim.y * blockIdx.z);
     return rb;
 }
 
@@ -114,8 +117,8 @@ __device__ __forceinline__ int physical_page(const int32_t* block_table, int b,
 }
 
 // ---- split slots of a batch -------------------------------------------------------------------
-// The plan's C = batch * Hkv * S split slots (one CTA each) are shared out among the (sequence,
-// KV head) units so that the busiest slot has as few 128-key tiles as possible. With w_b =
+// The plan's C split slots (one CTA each; as many as the GPU runs at once unless the split
+// count is forced, then batch * Hkv * S) are shared out among the (sequence, KV head) units so that the busiest slot has as few 128-key tiles as possible. With w_b =
 // ceil(n_b / 128) tiles in sequence b, T is the smallest tile count with
 //   Hkv * sum_b ceil(w_b / T) <= C,
 // and each KV head of sequence b owns c_b = ceil(w_b / T) contiguous slots, unit u = b * Hkv + h
@@ -169,7 +172,7 @@ __device__ __forceinline__ UnitSlots locate_slots_single(const int32_t* context_
 // the same arguments and gets the same result. by_slot: the unit owning slot key; else the slots
 // of unit key.
 __device__ __forceinline__ UnitSlots locate_slots_batch_body(const int32_t* context_lens,
-                                                             int B, int Hkv, int S,
+                                                             int B, int Hkv, int num_slots,
                                                              int max_context, int q_len,
                                                              int key, bool by_slot) {
     const int lane = threadIdx.x & 31;
@@ -199,7 +202,7 @@ __device__ __forceinline__ UnitSlots locate_slots_batch_body(const int32_t* cont
     if (W == 0) return r;
     // T: binary search between W Hkv / C (no split can do better) and the first count that is
     // surely enough, W Hkv / (C - U) (U = Hkv E: each unit's last split may be short), or wmax
-    const long long C = (long long)B * Hkv * S, U = (long long)Hkv * E;
+    const long long C = num_slots, U = (long long)Hkv * E;
     long long lo = (W * Hkv + C - 1) / C;
     long long hi = wmax;
     if (C > U) hi = min(hi, (W * Hkv + (C - U) - 1) / (C - U));
@@ -250,18 +253,27 @@ __device__ __forceinline__ UnitSlots locate_slots_batch_body(const int32_t* cont
 }
 
 static __device__ __noinline__ UnitSlots locate_slots_batch(const int32_t* context_lens, int B,
-                                                            int Hkv, int S, int max_context,
-                                                            int q_len, int key, bool by_slot) {
-    return locate_slots_batch_body(context_lens, B, Hkv, S, max_context, q_len, key, by_slot);
+                                                            int Hkv, int num_slots,
+                                                            int max_context, int q_len, int key,
+                                                            bool by_slot) {
+    return locate_slots_batch_body(context_lens, B, Hkv, num_slots, max_context, q_len, key,
+                                   by_slot);
 }
 
 // The slots of a unit or the unit of a slot (see above). Warp-cooperative. The several-sequence
 // search is called out of line: it runs once per CTA, and the kernels' hot code stays compact.
 __device__ __forceinline__ UnitSlots locate_slots(const int32_t* context_lens, int B, int Hkv,
-                                                  int S, int max_context, int q_len, int key,
-                                                  bool by_slot) {
+                                                  int S, int num_slots, int max_context,
+                                                  int q_len, int key, bool by_slot) {
     if (B == 1) return locate_slots_single(context_lens, Hkv, S, max_context, q_len, key, by_slot);
-    return locate_slots_batch(context_lens, B, Hkv, S, max_context, q_len, key, by_slot);
+    return locate_slots_batch(context_lens, B, Hkv, num_slots, max_context, q_len, key, by_slot);
+}
+
+// Grid of a partial launch: (splits x row blocks, Hkv, 1) for a single sequence, (slots x row
+// blocks, 1, 1) for a batch.
+inline dim3 partial_grid(const PartialParams& p) {
+    return p.batch == 1 ? dim3(p.num_splits * p.row_blocks, p.num_kv_heads, 1)
+                        : dim3(p.num_slots * p.row_blocks, 1, 1);
 }
 
 }  // namespace dflash

@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kSimtThreads, 1) simt_partial_kernel(PartialPa
     const RowBlock rb = row_block(p);
     const int G = p.group, R = rb.rows, row_lo = rb.row_lo, slot = rb.slot;
     const UnitSlots us = locate_slots(p.context_lens, p.batch, p.num_kv_heads, p.num_splits,
-                                      p.max_context, p.q_len, slot, true);
+                                      p.num_slots, p.max_context, p.q_len, slot, true);
     if (slot == 0 && tid == 0 && us.flags) atomicOr(p.status, us.flags);
     const int b = us.b, h = us.h, split = slot - us.first, n = us.n;
     if (b < 0) return;
@@ -179,7 +179,7 @@ cudaError_t launch_simt_partial(const PartialParams& p, cudaStream_t stream) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (!row_blocks_valid(p, kSimtRows)) return cudaErrorInvalidValue;
-    dim3 grid(p.num_splits * p.row_blocks, p.num_kv_heads, p.batch);
+    const dim3 grid = partial_grid(p);
     simt_partial_kernel<<<grid, kSimtThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }

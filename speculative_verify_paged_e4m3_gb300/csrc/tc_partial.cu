@@ -336,14 +336,15 @@ __device__ __forceinline__ void fused_merge(const PartialParams& p, uint8_t* sme
     c.rows = p.rows;
     c.max_context = p.max_context;
     c.num_splits = p.num_splits;
+    c.num_slots = p.num_slots;
     c.tile_keys = p.tile_keys;
     c.min_split_keys = p.min_split_keys;
     CombineScratch& sh = reinterpret_cast<CombineScratch*>(smem)[half];
     for (int it = first; it < items; it += workers) {
         const int quarter = it % kQuarters, r = (it / kQuarters) % p.rows;
         const int unit = it / (kQuarters * p.rows);
-        const UnitSlots us = locate_slots(p.context_lens, p.batch, p.num_kv_heads,
-                                          p.num_splits, p.max_context, p.q_len, unit, false);
+        const UnitSlots us = locate_slots(p.context_lens, p.batch, p.num_kv_heads, p.num_splits,
+                                          p.num_slots, p.max_context, p.q_len, unit, false);
         combine_item(c, r, quarter, unit / p.num_kv_heads, unit % p.num_kv_heads,
                      threadIdx.x % kCombineThreads, 1 + half, sh, us.first, us.count, us.n);
     }
@@ -378,7 +379,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                                  (rblk.xs * per_max + tid * kChunk) / P];
     const int slot = rblk.slot;
     const UnitSlots us = locate_slots(p.context_lens, p.batch, p.num_kv_heads, p.num_splits,
-                                      p.max_context, p.q_len, slot, true);
+                                      p.num_slots, p.max_context, p.q_len, slot, true);
     if (slot == 0 && tid == 0 && us.flags) atomicOr(p.status, us.flags);
     const int b = us.b, h = us.h, split = slot - us.first, n = us.n;
     const int per = b >= 0 ? keys_per_split(n, us.count, p.tile_keys, p.min_split_keys) : 1;
@@ -1056,7 +1057,7 @@ static cudaError_t launch_rp(const CUtensorMap& kmap, const CUtensorMap& vmap,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.num_splits * p.row_blocks, p.num_kv_heads, p.batch);
+    cfg.gridDim = partial_grid(p);
     cfg.blockDim = dim3(tc::Cfg<RP>::kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;

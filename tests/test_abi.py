@@ -128,6 +128,16 @@ def test_plan_row_blocks_fused(B):
     assert 4 * plan.row_blocks * plan.num_splits <= 152
 
 
+@pytest.mark.parametrize("batch,slots", [(1, 151), (1, 0), (4, 15), (4, 0)])
+def test_plan_num_slots_tampered(B, batch, slots):
+    # a single sequence's slots are Hkv * num_splits; a batch needs one per unit at least
+    plan = B.dflash_verify_attn_plan(problem(B, batch=batch, num_q_heads=24, num_kv_heads=4))
+    plan.num_slots = slots
+    with pytest.raises(B.DflashError) as e:
+        B.dflash_verify_attn_split_slots(plan, [1000] * batch)
+    assert e.value.status == B.DFLASH_ERR_INVALID_ARGUMENT
+
+
 @pytest.mark.parametrize("row_blocks", [0, -1, 1, 97])
 def test_plan_row_blocks_tampered(B, row_blocks):
     # a plan whose row blocks do not cover R in blocks the kernel can hold is refused
@@ -137,6 +147,31 @@ def test_plan_row_blocks_tampered(B, row_blocks):
     with pytest.raises(B.DflashError) as e:
         B.dflash_verify_attn_split_slots(plan, lens)
     assert e.value.status == B.DFLASH_ERR_INVALID_ARGUMENT
+
+
+@pytest.mark.parametrize("batch,hkv,q_len,splits,fused,slots", [
+    (1, 1, 8, 0, False, 152),      # one sequence: Hkv * num_splits
+    (1, 4, 8, 0, False, 152),
+    (4, 4, 8, 0, False, 152),      # a batch: every SM (16 * 9 = 144 would leave 8 idle)
+    (8, 4, 8, 0, False, 152),      # 32 * 4 = 128 would leave 24 idle
+    (4, 4, 16, 0, False, 76),      # two row blocks: 76 slots x 2 CTAs
+    (4, 4, 8, 0, True, 152),       # fused: still one CTA per SM
+    (4, 4, 8, 5, False, 80),       # forced split count: units * S
+    (200, 1, 8, 0, False, 200),    # more units than SMs: one slot each
+])
+def test_plan_num_slots(B, batch, hkv, q_len, splits, fused, slots):
+    pr = problem(B, batch=batch, num_q_heads=6 * hkv, num_kv_heads=hkv, q_len=q_len,
+                 num_splits=splits)
+    if fused:
+        pr.flags = B.DFLASH_PROBLEM_FUSED_COMBINE
+    plan = B.dflash_verify_attn_plan(pr)
+    assert plan.num_slots == slots
+    assert plan.num_slots * plan.row_blocks <= max(152, batch * hkv * plan.row_blocks)
+    R = plan.rows
+    assert plan.workspace_bytes >= plan.ws_acc_offset + slots * R * 256 * 4
+    assert plan.ws_acc_offset >= plan.ws_state_offset + slots * R * 8
+    if batch == 1:
+        assert slots == hkv * plan.num_splits
 
 
 @pytest.mark.parametrize("n", [0, 1, 7, 8, 100, 1024, 32768, 131072, 261888, 262144, 300000])
@@ -271,7 +306,7 @@ def test_default_split_count_fills_one_wave(B):
 def test_split_slots_layout(B):
     """Slots go to (sequence, KV head) units so that the busiest split is as short as possible:
     equal lengths here give num_splits slots each (the [batch, Hkv, S] layout), every non-empty
-    unit gets at least one, an empty unit none, and they fit in batch * Hkv * num_splits."""
+    unit gets at least one, an empty unit none, and they fit in the plan's num_slots."""
     plan = B.dflash_verify_attn_plan(problem(B, batch=4, num_q_heads=24, num_kv_heads=4,
                                              max_pages_per_seq=4096, num_pages=20000,
                                              max_context=65536))
@@ -283,20 +318,20 @@ def test_split_slots_layout(B):
     lens = [65536, 57344, 0, 40960]
     start, per, act = B.dflash_verify_attn_split_slots(plan, lens)
     cnt = [start[u + 1] - start[u] for u in range(units)]
-    assert start[0] == 0 and start[-1] <= units * S and all(c >= 0 for c in cnt)
+    assert start[0] == 0 and start[-1] <= plan.num_slots and all(c >= 0 for c in cnt)
     for u in range(units):
         n = lens[u // 4]
         assert (cnt[u] == 0) == (n == 0) and (act[u] == 0) == (n == 0)
         if n:
             assert act[u] <= cnt[u] and per[u] * act[u] >= n > per[u] * (act[u] - 1)
-    share = [cnt[u] / (units * S) for u in range(units)]
+    share = [cnt[u] / plan.num_slots for u in range(units)]
     total = 4 * sum(lens)
     for u in range(units):
         if lens[u // 4]:
-            assert abs(share[u] - lens[u // 4] / total) * units * S <= 1.5
+            assert abs(share[u] - lens[u // 4] / total) * plan.num_slots <= 1.5
     # the longest split is no longer than about the average
     tiles = [math.ceil(p / 128) for p, a in zip(per, act) if a]
-    assert max(tiles) <= math.ceil(sum(math.ceil(n / 128) for n in lens) * 4 / (units * S)) + 2
+    assert max(tiles) <= math.ceil(sum(math.ceil(n / 128) for n in lens) * 4 / plan.num_slots) + 2
 
 
 @pytest.mark.parametrize("lens", [
@@ -311,7 +346,7 @@ def test_split_slots_min_max_rule(B, lens):
     Hkv = 4
     plan = B.dflash_verify_attn_plan(problem(B, batch=len(lens), num_q_heads=24, num_kv_heads=Hkv,
                                              max_pages_per_seq=16384, num_pages=20000))
-    C = len(lens) * Hkv * plan.num_splits
+    C = plan.num_slots
     w = [math.ceil(min(max(n, 0), 262144) / 128) for n in lens]
     T = next(t for t in range(1, max(w) + 1)
              if Hkv * sum(math.ceil(x / t) for x in w) <= C)
