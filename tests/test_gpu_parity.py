@@ -282,15 +282,33 @@ def test_fused_barrier_reused_across_grid_sizes():
         assert att.workspace_views()[0].item() == 0
 
 
-def test_ragged_batch_slots_match_host_layout():
-    """A ragged batch (one sequence empty): the partial kernel writes state into exactly the
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("batch", [33, 70])
+def test_batch_beyond_one_warp_of_sequences(kernel, batch):
+    # more sequences than a warp's lanes: the slot search runs over several 32-sequence chunks
+    rng = np.random.default_rng(batch)
+    lens = [int(x) for x in rng.integers(0, 700, size=batch)]
+    lens[0], lens[batch // 2], lens[-1] = 0, 900, 17
+    lens = [max(n, 8) if n else 0 for n in lens]  # a length below q_len is covered elsewhere
+    att, *_ = check(small(f"b{batch}", lens, seed=batch), kernel)
+    from speculative_verify_paged_e4m3_gb300 import binding as B
+    start, per, act = B.dflash_verify_attn_split_slots(att.plan, lens)
+    assert start[-1] <= att.plan.num_slots and sum(1 for a in act if a) == sum(1 for n in lens if n)
+
+
+@pytest.mark.parametrize("lens,Hkv", [
+    ([3000, 700, 0, 1600], 2),
+    ([(37 * i) % 1500 for i in range(70)], 1),  # several 32-sequence chunks, some empty
+])
+def test_ragged_batch_slots_match_host_layout(lens, Hkv):
+    """A ragged batch (some sequences empty): the partial kernel writes state into exactly the
     slots the host-side layout (dflash_verify_attn_split_slots) lists, and nothing else."""
     from speculative_verify_paged_e4m3_gb300 import binding as B
-    w = small("slots", [3000, 700, 0, 1600], Hq=12, Hkv=2, seed=51)
+    w = small("slots", lens, Hq=6 * Hkv, Hkv=Hkv, seed=51)
     inp = W.make_layer(w, 0, device="cpu")
     dev = to_device(inp)
     q = dev["q"]
-    att = B.VerifyAttention(q.shape[0], q.shape[1], q.shape[2], 2, 256, 16,
+    att = B.VerifyAttention(q.shape[0], q.shape[1], q.shape[2], Hkv, 256, 16,
                             dev["block_table"].shape[1], dev["k_pool"].shape[0], w.max_ctx,
                             device=0)
     _, state, _ = att.workspace_views()
