@@ -83,7 +83,7 @@ constexpr uint32_t kChunkBytes = kChunk * kHeadDim;  // 4096
 constexpr uint32_t kGroupStride = 2048;              // 8 keys x both halves
 constexpr uint32_t kHalfOffset = 1024;               // 8 keys x 128 bytes
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
-constexpr int kRowCache = 128;  // 16-key chunks of a split whose source row is looked up up front
+constexpr int kRowCache = 512;  // 16-key chunks of a split whose source row is looked up up front
 constexpr float kPShift = 4.f;         // s: probabilities are scaled by 2^s before the split
 constexpr float kLazyThreshold = 8.f;  // largest shifted probability exponent, 8 - s above the max
 
@@ -230,9 +230,9 @@ __device__ __forceinline__ bool group_sync(const Ctx& ctx, int g, int wq, int& e
     return group_wait(ctx, g, group_arrive(ctx, g, wq, epoch, vote), any);
 }
 
-// (pool row, clamped?) of key j0 of sequence b from the block table; out of line, as splits
-// longer than the row cache are rare
-__device__ __noinline__ int2 table_row(const int32_t* block_table, int b, int max_pages_per_seq,
+// (pool row, clamped?) of key j0 of sequence b from the block table (splits longer than the
+// row cache: inline, so that a copier's lookups for one stage are all in flight together)
+__device__ __forceinline__ int2 table_row(const int32_t* block_table, int b, int max_pages_per_seq,
                                        int page_size, int num_pages, int j0) {
     bool clamped = false;
     const int phys = physical_page(block_table, b, max_pages_per_seq, j0 / page_size, num_pages,
