@@ -63,6 +63,13 @@ def test_forced_split_counts(kernel, splits):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("splits,n,P", [(1, 20000, 16), (2, 33000, 64), (3, 26000, 32)])
+def test_splits_longer_than_row_cache(kernel, splits, n, P):
+    # more than 512 16-key chunks per split: chunks past the row cache come from the block table
+    check(small(f"long{splits}", [n], P=P, seed=300 + splits), kernel, num_splits=splits)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("P,n", [(16, 777), (32, 1000), (48, 999), (64, 2049), (3296, 7000),
                                  (16, 128), (16, 129), (16, 255), (16, 256)])
 def test_page_sizes(kernel, P, n):
