@@ -144,6 +144,8 @@ def pin_tiny_vs_torch_sdpa(orc):
         dict(q_len=5, Hq=4, Hkv=2, D=16, P=3, contexts=(5, 23)),
         dict(q_len=3, Hq=2, Hkv=2, D=32, P=16, contexts=(64, 9, 33)),
         dict(q_len=8, Hq=6, Hkv=1, D=256, P=64, contexts=(8,)),
+        dict(q_len=16, Hq=6, Hkv=1, D=256, P=16, contexts=(40,)),   # 96 rows per KV head
+        dict(q_len=16, Hq=16, Hkv=1, D=32, P=16, contexts=(50, 16)),  # 256 rows per KV head
     ]
     for sh in shapes:
         case = paged_case(rng, B=len(sh["contexts"]), **sh)
@@ -287,10 +289,10 @@ def pin_split_merge_exact_integers(orc):
     assert np.array_equal(l1[0, 0, 0].reshape(q_len, 6)[:, 0], n_vis.astype(np.float64))
 
 
-def pin_q1_reduction(orc):
+def pin_q1_reduction(orc, q_len=8, seed=31):
     """Token i of a q_len block equals a q_len = 1 call over the first N - q_len + i + 1 keys."""
-    rng = np.random.default_rng(31)
-    N, q_len = 75, 8
+    rng = np.random.default_rng(seed)
+    N = 75
     case = paged_case(rng, q_len=q_len, Hq=6, Hkv=1, D=256, contexts=(N,))
     out, lse = run(orc, case)
     for i in range(q_len):
@@ -299,6 +301,11 @@ def pin_q1_reduction(orc):
         one["context_lens"] = np.array([N - q_len + i + 1], dtype=np.int32)
         o1, l1 = run(orc, one)
         assert np.array_equal(o1[:, 0], out[:, i]) and np.array_equal(l1[:, 0], lse[:, i]), i
+
+
+def pin_q1_reduction_long_block(orc):
+    """The same reduction for a 16-token block (more rows than one tensor-core CTA holds)."""
+    pin_q1_reduction(orc, q_len=16, seed=32)
 
 
 def _spec_points():
@@ -458,6 +465,7 @@ PINS = [
     pin_split_merge_agreement,
     pin_split_merge_exact_integers,
     pin_q1_reduction,
+    pin_q1_reduction_long_block,
     pin_e4m3_encode_spec_points,
     pin_e4m3_encode_midpoints_ties_to_even,
     pin_e4m3_encode_vs_torch_cast,
