@@ -166,8 +166,8 @@ int dflash_verify_attn_split_slots(const dflash_verify_attn_plan_t* plan,
                                    int32_t* keys_per_split, int32_t* active);
 
 /*
- * Split boundaries the kernels use when every sequence of the batch has context length n (then
- * every unit owns num_splits slots, dflash_verify_attn_split_slots): keys_per_split =
+ * Split boundaries the kernels use for a single sequence of context length n, whose KV heads
+ * own num_splits slots each (for a batch, dflash_verify_attn_split_slots): keys_per_split =
  * roundup(max(ceil(n / S), min_split_keys), tile_keys), split s covers
  * [s * keys_per_split, min(n, (s + 1) * keys_per_split)), and the first
  * *active = ceil(n / keys_per_split) splits are non-empty (0 when n == 0). n is clamped to
@@ -199,8 +199,9 @@ int dflash_verify_attn_combine(const dflash_verify_attn_plan_t* plan, const void
                                float* lse, void* cuda_stream);
 
 /*
- * run followed by combine on one stream. With DFLASH_PROBLEM_FUSED_COMBINE in problem.flags (tensor-core kernel, batch * num_kv_heads <=
- * the SM count; plan->combine_fused tells), both happen in a single cooperative launch of the
+ * run followed by combine on one stream. With DFLASH_PROBLEM_FUSED_COMBINE in problem.flags
+ * (tensor-core kernel, batch * num_kv_heads * row_blocks <= the SM count; plan->combine_fused
+ * tells), both happen in a single cooperative launch of the
  * partial kernel instead: after every CTA has written its split state (a bounded grid-wide
  * barrier on the workspace header), the CTAs share out the combine's work and write out and lse
  * themselves. Results match run + combine within the output tolerance, and are the same bits
