@@ -1,7 +1,7 @@
 """Shared helpers of the GPU parity tests: run the CUDA path through the C ABI, run the oracle on
 the same inputs, and compare with the stated tolerances.
 
-Tolerances (BASELINE's acceptance, read as below):
+Tolerances (the acceptance bar for this operator, read as below):
   * out: |gpu - exact| <= 2e-3 + half an FP16 ulp of the exact value. The 2e-3 bounds the
     arithmetic; the output format's own rounding (up to 2^-9 for |out| in [4, 8)) is added on top
     so that a correctly computed value that rounds to the neighbouring FP16 is not called wrong.
