@@ -61,7 +61,8 @@ int check_plan(const dflash_verify_attn_plan_t* plan) {
     // slots: Hkv * num_splits for a single sequence (the grid (S, Hkv, 1)); at least one per
     // unit for a batch
     const int64_t units = (int64_t)plan->problem.batch * plan->problem.num_kv_heads;
-    if (plan->problem.batch < 1 || plan->problem.num_kv_heads < 1) return DFLASH_ERR_INVALID_ARGUMENT;
+    if (plan->problem.batch < 1 || plan->problem.num_kv_heads < 1)
+        return DFLASH_ERR_INVALID_ARGUMENT;
     if (plan->problem.batch == 1 ? plan->num_slots != units * plan->num_splits
                                  : plan->num_slots < units)
         return DFLASH_ERR_INVALID_ARGUMENT;

@@ -118,8 +118,9 @@ __device__ __forceinline__ int physical_page(const int32_t* block_table, int b,
 
 // ---- split slots of a batch -------------------------------------------------------------------
 // The plan's C split slots (one CTA each; as many as the GPU runs at once unless the split
-// count is forced, then batch * Hkv * S) are shared out among the (sequence, KV head) units so that the busiest slot has as few 128-key tiles as possible. With w_b =
-// ceil(n_b / 128) tiles in sequence b, T is the smallest tile count with
+// count is forced, then batch * Hkv * S) are shared out among the (sequence, KV head) units so
+// that the busiest slot has as few 128-key tiles as possible. With w_b = ceil(n_b / 128) tiles
+// in sequence b, T is the smallest tile count with
 //   Hkv * sum_b ceil(w_b / T) <= C,
 // and each KV head of sequence b owns c_b = ceil(w_b / T) contiguous slots, unit u = b * Hkv + h
 // from slot Hkv * (c of the sequences before b) + h * c_b; the slots past all units stay idle.
@@ -186,8 +187,8 @@ __device__ __forceinline__ UnitSlots locate_slots_batch_body(const int32_t* cont
     int wmax = 0, E = 0, flags = 0;
     for (int b0 = 0; b0 < B; b0 += 32) {
         const int b = b0 + lane;
-        const int w = b < B ? slot_granules(slot_length(context_lens, b, max_context, q_len, &flags))
-                            : 0;
+        const int w =
+            b < B ? slot_granules(slot_length(context_lens, b, max_context, q_len, &flags)) : 0;
         W += w;
         wmax = max(wmax, w);
         E += w > 0;

@@ -127,7 +127,8 @@ __global__ void __launch_bounds__(kSimtThreads, 1) simt_partial_kernel(PartialPa
         for (int d = 0; d < kHeadDim; ++d) {
             const float kv = Ks[lane * kKStride + d];
 #pragma unroll
-            for (int m = 0; m < kSimtRows / 8; ++m) s[m] = fmaf(Qs[(warp + 8 * m) * kHeadDim + d], kv, s[m]);
+            for (int m = 0; m < kSimtRows / 8; ++m)
+                s[m] = fmaf(Qs[(warp + 8 * m) * kHeadDim + d], kv, s[m]);
         }
         const int j = t0 + lane;
 #pragma unroll

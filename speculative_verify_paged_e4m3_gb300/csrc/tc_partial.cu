@@ -119,7 +119,7 @@ struct Small {
     uint32_t tmem_base;
     int abort;
     int gvote[kMaxRP / kGroupRows][2][4];  // group votes: [group][phase parity][warp]
-    alignas(16) float c0[kMaxRP];  // score scale of each row (log2 units per MMA unit), float4 reads
+    alignas(16) float c0[kMaxRP];  // score scale of each row (log2 units per MMA unit), as float4
     float rmax[kMaxRP / kGroupRows][4][kGroupRows];  // per-group, per-warp row maxima of a tile
     float rsum[kMaxRP / kGroupRows][4][kGroupRows];  // per-group, per-warp row sums of the split
     int rows[kRowCache];  // source row (physical page * page + slot) of chunk c of the split
@@ -310,7 +310,8 @@ template <int NT>
 __device__ __forceinline__ void fused_merge(const PartialParams& p, uint8_t* smem) {
     constexpr int kHalves = NT / kCombineThreads;
     constexpr int kQuarters = kHeadDim / (4 * kCombineCols);
-    volatile int* barrier_ok = reinterpret_cast<volatile int*>(smem + kHalves * sizeof(CombineScratch));
+    volatile int* barrier_ok =
+        reinterpret_cast<volatile int*>(smem + kHalves * sizeof(CombineScratch));
     const int half = threadIdx.x / kCombineThreads;
     const int cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
     const int workers = gridDim.x * gridDim.y * gridDim.z * kHalves;
@@ -625,7 +626,8 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                         const uint64_t ad = smem_desc(kb + (kk >> 2) * kHalfOffset + (kk & 3) * 32,
                                                       16, kGroupStride, kSwizzle128B);
                         const uint64_t bd = smem_desc(
-                            q_base + (kk >> 2) * (SN * 128) + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+                            q_base + (kk >> 2) * (SN * 128) + (kk & 3) * 32, 16, 1024,
+                            kSwizzle128B);
                         mma_f8_ss(tmem + C::kColS, ad, bd, idesc_qk, kk > 0);
                     }
                     mma_commit(smem_u32(&sm.kempty[s]));
@@ -871,8 +873,8 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             }
             bool ok = true;
             if (need_any) {
-                // exact tile maximum per row -> new reference max (every thread of the group derives
-                // the same values from the warps' partial maxima); rescale row sums and O
+                // exact tile maximum per row -> new reference max (every thread of the group
+                // derives the same values from the warps' partial maxima); rescale row sums and O
 #pragma unroll
                 for (int q = 0; q < kGroupRows / 2; ++q) {
                     const float m0 = warp_max(((validm >> (2 * q)) & 1u) ? lo2(y[q]) : -INFINITY);
@@ -979,7 +981,8 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                 }
             }
         }
-        // O^T (tensor memory, lane = head-dim element) -> numerator rows: O = O_h + O_m/16 + O_l/256
+        // O^T (tensor memory, lane = head-dim element) -> numerator rows:
+        // O = O_h + O_m/16 + O_l/256
         const bool ok = ctx.wait_warp(&sm.odone, 0);
         tc_fence_after();
         if (__all_sync(0xffffffffu, ok && !ctx.aborted())) {
