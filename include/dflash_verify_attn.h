@@ -135,7 +135,10 @@ typedef struct {
 } dflash_verify_attn_plan_t;
 
 /*
- * Check the problem and choose the split count, tile and kernel for it. Host only; queries the
+ * Check the problem and choose the split count, tile and kernel for it. The context is cut into
+ * logical splits ("[Perf] Reduce DFlash2 long-context verification decay", Implementation: 80
+ * logical splits, sized there to the V100's 80 SMs); here the split count follows this GPU's SM
+ * count and the keys per split follow the live context length. Host only; queries the
  * device's SM count (cudaDeviceGetAttribute) unless problem->device < 0, in which case a
  * 152-SM part is assumed (lets plans be built and checked without a GPU).
  * Returns DFLASH_ERR_INVALID_ARGUMENT for a malformed problem, DFLASH_ERR_UNSUPPORTED for a
@@ -179,7 +182,10 @@ int dflash_verify_attn_split_bounds(const dflash_verify_attn_plan_t* plan, int32
 
 /*
  * Partial attention: for every (sequence, KV head, active split) write the split's FP32 state
- * (m, l, numerator) into the workspace. Inputs as in the layout table above. workspace_bytes must
+ * (m, l, numerator) into the workspace ("[Perf] Reduce DFlash2 attention cost and screen exact QK
+ * reuse", Purpose: the complete FP32 numerator / max / sum workspace; "[Perf] Reduce DFlash2
+ * long-context verification decay", Implementation: one CTA carries every query head of its KV
+ * head, so each K/V page is read once). Inputs as in the layout table above. workspace_bytes must
  * be >= plan->workspace_bytes and the workspace 256-byte aligned; q, k_pool and v_pool must be
  * 16-byte aligned. cuda_stream is a cudaStream_t (NULL: legacy default stream).
  */
@@ -191,15 +197,19 @@ int dflash_verify_attn_run(const dflash_verify_attn_plan_t* plan, const void* q,
 
 /*
  * Combine: merge the active splits' state of every query row into out (FP16, round to nearest
- * even) and lse (FP32, natural log). Must follow dflash_verify_attn_run on the same stream with
- * the same plan, workspace and context_lens.
+ * even) and lse (FP32, natural log): M = max_s m_s, L = sum_s e^{m_s - M} l_s,
+ * out = sum_s e^{m_s - M} acc_s / L, lse = M + ln L ("[Perf] Reduce DFlash2 attention cost and
+ * screen exact QK reuse", Test Result: each grouped q8 attention kernel is followed by one
+ * combine kernel). Must follow dflash_verify_attn_run on the same stream with the same plan,
+ * workspace and context_lens.
  */
 int dflash_verify_attn_combine(const dflash_verify_attn_plan_t* plan, const void* workspace,
                                size_t workspace_bytes, const int32_t* context_lens, void* out,
                                float* lse, void* cuda_stream);
 
 /*
- * run followed by combine on one stream. With DFLASH_PROBLEM_FUSED_COMBINE in problem.flags
+ * run followed by combine on one stream: the per-layer pair of "[Perf] Reduce DFlash2 attention
+ * cost and screen exact QK reuse", Test Result. With DFLASH_PROBLEM_FUSED_COMBINE in problem.flags
  * (tensor-core kernel, batch * num_kv_heads * row_blocks <= the SM count; plan->combine_fused
  * tells), both happen in a single cooperative launch of the
  * partial kernel instead: after every CTA has written its split state (a bounded grid-wide
@@ -238,10 +248,13 @@ int dflash_verify_attn_kv_write(const dflash_verify_attn_plan_t* plan, const voi
                                 void* workspace, size_t workspace_bytes, void* cuda_stream);
 
 /*
- * Debug export of the kernels' E4M3 decode (the same device function the tensor-core kernel uses
- * for K and V): decoded[t] = exact value of codes[t] (NaN for S.1111.111), scaled[t] =
- * decoded[t] * *scale rounded once to FP32. n >= 0 elements; all pointers device memory;
- * scaled may be NULL.
+ * Debug export of an E4M3 decode: the two-code hardware conversion (cvt.rn.f16x2.e4m3x2) that the
+ * CUDA-core kernel uses for K and V and the tensor-core kernel uses for the residuals of its Q
+ * split. (The tensor-core kernel hands K and V codes to the tensor core undecoded; its decode is
+ * checked through the attention outputs of one-key problems instead.) decoded[t] = exact value
+ * of codes[t] (NaN for S.1111.111), scaled[t] = decoded[t] * *scale rounded once to FP32
+ * ("[Perf] Add opt-in DFlash2 schedules and numerical audits", Test Plan: E4M3 target KV).
+ * n >= 0 elements; all pointers device memory; scaled may be NULL.
  */
 int dflash_verify_attn_debug_dequant(const uint8_t* codes, int64_t n, const float* scale,
                                      float* decoded, float* scaled, void* cuda_stream);
@@ -262,9 +275,13 @@ int dflash_verify_attn_read_flags(const void* workspace, int32_t* flags_host, in
  * Limits and behaviour: plan->workspace_bytes must be <= 16 MiB, else
  * DFLASH_ERR_WORKSPACE_TOO_SMALL and nothing is launched. The first call on a device (with that
  * device current) looks up the array's device address once; make it before any stream capture.
- * All calls share the array: the status word at its head is zeroed at the start of each call and
- * is not reported, and calls whose kernels overlap on the GPU race on the array. The array stays
- * allocated on every device that loaded the library until the process exits.
+ * All calls share the array. The first 16 bytes of its header (the status word and the fused
+ * merge's grid-barrier counter) are zeroed on the stream at the start of each call, so no call
+ * inherits a barrier count from an earlier one. The status word is not reported on this path:
+ * a clamped context or page entry goes unseen, and after a kernel wait that gave up
+ * (DFLASH_FLAG_KERNEL_TIMEOUT on the ordinary entry points) out and lse are undefined. Calls
+ * whose kernels overlap on the GPU race on the array. The array stays allocated on every device
+ * that loaded the library until the process exits.
  */
 int dflash_verify_attn_forward_static_scratch(const dflash_verify_attn_plan_t* plan,
                                               const void* q, const void* k_pool,

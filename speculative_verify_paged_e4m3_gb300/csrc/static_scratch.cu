@@ -11,10 +11,14 @@
 // until the process exits. Host code cannot use its name as a device address (on the host the
 // name refers to a host-side stand-in), so the first call on each device, with that device
 // current, looks the address up once with cudaGetSymbolAddress and caches it; make that first
-// call before any stream capture. Every call shares the one array: the status word at its head
-// is cleared on the stream at the start of each call (the split state needs no clearing; each
-// active split is written before the combine reads it), and two calls whose kernels overlap on
-// the GPU -- on different streams, say -- race on it.
+// call before any stream capture. Every call shares the one array. At the start of each call the
+// first 16 bytes of its header are cleared on the stream: the status word and the ticket counter
+// of the fused merge's grid barrier, so that a call never inherits a count that an earlier,
+// timed-out or overlapping fused call left behind. The split state is not cleared: when every
+// wait of the kernels completes, each active split is written before the merge reads it. The
+// status word is not reported on this path, so a wait that gives up (DFLASH_FLAG_KERNEL_TIMEOUT)
+// goes unseen, and out and lse of that call are undefined. Two calls whose kernels overlap on
+// the GPU -- on different streams, say -- race on the array.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -25,6 +29,8 @@ namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB
 constexpr int kMaxDevices = 64;
+// status word (offset 0) and the fused merge's 64-bit grid-barrier ticket counter (offset 8)
+constexpr size_t kClearedHeaderBytes = 16;
 
 static __device__ __align__(256) unsigned char g_verify_attn_scratch[kStaticScratchBytes];
 
@@ -60,7 +66,7 @@ extern "C" int dflash_verify_attn_forward_static_scratch(
         scratch = g_scratch_address[dev];
     }
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-    if (cudaMemsetAsync(scratch, 0, sizeof(int32_t), stream) != cudaSuccess) {
+    if (cudaMemsetAsync(scratch, 0, kClearedHeaderBytes, stream) != cudaSuccess) {
         cudaGetLastError();
         return DFLASH_ERR_CUDA;
     }
