@@ -11,9 +11,13 @@
 //    and straight into the tensor core. Keys sit on the MMA's M dimension (M = 128 keys per tile)
 //    and query rows on N: S^T = K Q^T (K K-major) and O^T = V^T P^T (V read MN-major from the very
 //    same tile layout), so no MMA work is spent on padding rows.
-//  * Q (FP16) is split exactly into three E4M3 terms q * 2^a = t0 + t1/16 + t2/256 (per-row
-//    power-of-two a), stacked on N (N = 3 x rows); the score is (S0 + S1/16 + S2/256) * 2^-a *
-//    k_scale / 16 * log2 e.
+//  * Q (FP16) is split into three E4M3 terms q * 2^a = t0 + t1/16 + t2/256 (per-row power-of-two
+//    a, which puts the row's largest magnitude in (224, 448]), stacked on N (N = 3 x rows); the
+//    score is (S0 + S1/16 + S2/256) * 2^-a * k_scale / 16 * log2 e. Each residual is exact, so
+//    the split is exact for every element of at least 2^-7 after scaling (2^-15 of the row
+//    maximum): three 4-bit significands cover FP16's 11 bits. Smaller elements lose low bits to
+//    the third term's subnormal grid, an absolute error of at most 2^-18 after scaling, below
+//    2^-25 of the row maximum.
 //  * The probabilities, taken as p = 2^(s - m) * 2^score with s = 4 and a reference max m (so
 //    p <= 2^8, see below), are split the same way into three E4M3 terms p = h + m/16 + l/256
 //    (h and m truncated to 4 significant bits, residuals exact, l rounded: relative error about

@@ -1,4 +1,4 @@
-// tc_ptx.cuh -- inline-PTX wrappers for sm_103a: mbarriers, bulk async copies, tensor memory
+// tc_ptx.cuh -- inline-PTX wrappers for sm_103a: mbarriers, TMA tensor copies, tensor memory
 // (tcgen05.alloc / ld / st), tcgen05.mma with shared-memory matrix descriptors, and fences.
 //
 // Descriptor formats (PTX ISA, tcgen05 "shared memory descriptor" and "instruction descriptor"):
@@ -75,26 +75,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
     }
 }
 
-// ---- bulk async copy (global -> shared, completes a transaction count on an mbarrier) ---------
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-// 2-D tiled tensor copy global -> shared through a TMA descriptor (box given by the map).
-// x is the innermost coordinate (elements), y the row; completes a transaction on bar.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tensor_map, int x, int y,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tensor_map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
 // Fetch a TMA descriptor (a kernel parameter) ahead of its first use.
 __device__ __forceinline__ void prefetch_tensormap(const void* tensor_map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tensor_map))
@@ -109,16 +89,6 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     return policy;
 }
 
-// tma_load_2d with an L2 cache policy for the copied lines.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tensor_map, int x, int y,
-                                            uint32_t bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tensor_map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
-        : "memory");
-}
-
 // 4-D tiled tensor copy global -> shared with an L2 cache policy; coordinates innermost first.
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tensor_map, int c0, int c1,
                                             int c2, int c3, uint32_t bar, uint64_t policy) {
@@ -128,10 +98,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tensor_map
         "l"(reinterpret_cast<uint64_t>(tensor_map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar),
         "l"(policy)
         : "memory");
-}
-
-__device__ __forceinline__ void named_barrier(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // 2^x, hardware approximation (relative error about 2^-22), subnormal results flushed.
@@ -243,27 +209,6 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
                  :
                  : "memory");
 }
-// 32 lanes x 8 consecutive 32-bit columns.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                   "=r"(r[6]), "=r"(r[7])
-                 : "r"(taddr));
-}
-// Wait for outstanding tcgen05.ld, threading n registers through the wait (n = 8, 16, 24, ...).
-template <int N>
-__device__ __forceinline__ void tmem_ld_wait_n(uint32_t* r) {
-    static_assert(N % 8 == 0, "multiple of 8 registers");
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                   "+r"(r[6]), "+r"(r[7])
-                 :
-                 : "memory");
-    if constexpr (N > 8) tmem_ld_wait_n<N - 8>(r + 8);
-}
-__device__ __forceinline__ void tmem_ld_wait() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -273,12 +218,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         "r"(r[15])
         : "memory");
 }
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
-                 ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
-                 "r"(r[6]), "r"(r[7])
-                 : "memory");
-}
 __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -286,8 +225,6 @@ __device__ __forceinline__ void tmem_st_wait() {
 // ---- descriptors -----------------------------------------------------------------------------
 constexpr uint32_t kSwizzleNone = 0;
 constexpr uint32_t kSwizzle128B = 2;
-constexpr uint32_t kSwizzle64B = 4;
-constexpr uint32_t kSwizzle32B = 6;
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo_bytes,
                                               uint32_t sbo_bytes, uint32_t swizzle) {
@@ -304,31 +241,13 @@ __host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, int a_type, in
 }
 
 // ---- MMA -------------------------------------------------------------------------------------
-// D[tmem] (+)= A[smem] * B[smem]^T, FP16 inputs, FP32 accumulate.
-__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                           uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// Same with 8-bit (E4M3) inputs.
+// D[tmem] (+)= A[smem] * B[smem]^T, 8-bit (E4M3) inputs, FP32 accumulate.
 __device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// A from tensor memory, B from shared memory, FP16 inputs.
-__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                           uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 // Arrive on an mbarrier once every tcgen05 operation this thread issued so far has completed.
