@@ -15,6 +15,7 @@ namespace dflash {
 template <int SL, bool kBatch>
 __global__ void __launch_bounds__(kCombineThreads) combine_lanes_kernel(CombineParams p) {
     __shared__ CombineScratch sh;
+    griddep_launch_dependents();  // the next kernel may start launching (programmatic launch)
     const int unit = blockIdx.z;
     const int b = unit / p.num_kv_heads, h = unit % p.num_kv_heads;
     int first, count, n;
@@ -35,15 +36,16 @@ __global__ void __launch_bounds__(kCombineThreads) combine_lanes_kernel(CombineP
 
 // Plans with few splits per unit (many units: a batch, whole-model heads) merge a whole row per
 // 64 threads instead: one CTA per (4 query rows, unit), each thread one float4 column across
-// all of the unit's splits. Same arithmetic as combine_item's final step (maximum, then weighted
-// sums in split order), which is all of combine_item when no split lane holds more than one
-// split: results are the same bits for up to 16 splits per unit.
+// all of the unit's splits: the maximum, then one rounded product per split added in split
+// order. That is combine_item's arithmetic when no split lane holds more than one split, so
+// results are the same bits for up to 16 splits per unit.
 constexpr int kRowCols = kHeadDim / 4;                 // 64 float4 columns per row
 constexpr int kRowsPerCta = kCombineThreads / kRowCols;  // 4
 constexpr int kRowKernelMaxSplits = kCombineSplitLanes;  // 16
 
 template <bool kBatch>
 __global__ void __launch_bounds__(kCombineThreads) combine_rows_kernel(CombineParams p) {
+    griddep_launch_dependents();  // the next kernel may start launching (programmatic launch)
     const int unit = blockIdx.y;
     const int r = blockIdx.x * kRowsPerCta + threadIdx.x / kRowCols;
     const int col = threadIdx.x % kRowCols;
@@ -66,6 +68,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_rows_kernel(CombinePa
     const int active = n > 0 ? (n + per - 1) / per : 0;
     const int R = p.rows;
     const float4* acc4 = reinterpret_cast<const float4*>(p.ws_acc);
+    griddep_wait();  // the split state only after the partial kernel has completed
     float M = -INFINITY;
     for (int s = 0; s < active; ++s)
         M = fmaxf(M, __ldcg(&p.ws_state[(int64_t)(first + s) * R + r]).x);
@@ -86,11 +89,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_rows_kernel(CombinePa
             for (int k = 0; k < kBatchLoads; ++k) {
                 if (s0 + k >= active) break;
                 const float w = st[k].x == -INFINITY ? 0.f : merge_ex2(st[k].x - M);
-                t.x = fmaf(w, a[k].x, t.x);
-                t.y = fmaf(w, a[k].y, t.y);
-                t.z = fmaf(w, a[k].z, t.z);
-                t.w = fmaf(w, a[k].w, t.w);
-                Lt = fmaf(w, st[k].y, Lt);
+                t.x = __fadd_rn(t.x, __fmul_rn(w, a[k].x));
+                t.y = __fadd_rn(t.y, __fmul_rn(w, a[k].y));
+                t.z = __fadd_rn(t.z, __fmul_rn(w, a[k].z));
+                t.w = __fadd_rn(t.w, __fmul_rn(w, a[k].w));
+                Lt = __fadd_rn(Lt, __fmul_rn(w, st[k].y));
             }
         }
         const float inv = 1.f / Lt;
@@ -107,29 +110,45 @@ __global__ void __launch_bounds__(kCombineThreads) combine_rows_kernel(CombinePa
     if (col == 0) p.lse[orow] = (M == -INFINITY) ? -INFINITY : (M + log2f(Lt)) * kLn2;
 }
 
+// One launch of kernel over grid, 256 threads; with p.pdl a programmatic dependent of the
+// preceding kernel on the stream.
+static cudaError_t launch(void (*kernel)(CombineParams), dim3 grid, const CombineParams& p,
+                          cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kCombineThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (p.pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 template <int SL>
-static void launch_lanes(const CombineParams& p, cudaStream_t stream) {
+static cudaError_t launch_lanes(const CombineParams& p, cudaStream_t stream) {
     const dim3 grid(p.rows, SL / 4, p.batch * p.num_kv_heads);
-    if (p.batch == 1)
-        combine_lanes_kernel<SL, false><<<grid, kCombineThreads, 0, stream>>>(p);
-    else
-        combine_lanes_kernel<SL, true><<<grid, kCombineThreads, 0, stream>>>(p);
+    return launch(p.batch == 1 ? combine_lanes_kernel<SL, false> : combine_lanes_kernel<SL, true>,
+                  grid, p, stream);
 }
 
 constexpr int kMidKernelMaxSplits = 64;
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
+    cudaError_t e;
     if (p.num_splits <= kRowKernelMaxSplits) {
         const dim3 grid((p.rows + kRowsPerCta - 1) / kRowsPerCta, p.batch * p.num_kv_heads);
-        if (p.batch == 1)
-            combine_rows_kernel<false><<<grid, kCombineThreads, 0, stream>>>(p);
-        else
-            combine_rows_kernel<true><<<grid, kCombineThreads, 0, stream>>>(p);
+        e = launch(p.batch == 1 ? combine_rows_kernel<false> : combine_rows_kernel<true>, grid, p,
+                   stream);
     } else if (p.num_splits <= kMidKernelMaxSplits) {
-        launch_lanes<4>(p, stream);
+        e = launch_lanes<4>(p, stream);
     } else {
-        launch_lanes<kCombineSplitLanes>(p, stream);
+        e = launch_lanes<kCombineSplitLanes>(p, stream);
     }
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
