@@ -39,9 +39,9 @@
 //    warps: on this GPU the copy throughput of one SM grows with the number of warps issuing them
 //    (measured with this very box pattern: 4.4, 6.2 and 6.6 TB/s over the whole GPU for one, two
 //    and three warps).
-//  * One P buffer, reused slice by slice: the softmax warp of lane quadrant q owns keys
-//    [32q, 32q + 32) of every tile, so it waits only for the PV step that read its slice of the
-//    previous tile; the MMAs of a V stage wait for the P slices they read.
+//  * One P buffer: the softmax warp of lane quadrant q writes keys [32q, 32q + 32) of every
+//    tile once the PV of the previous tile has read them; the PV of a tile waits for one
+//    barrier that every softmax warp arrives on (one test for the MMA thread to poll).
 //  * The softmax math runs on FP32 pairs (f32x2 instructions), the warpgroup barriers on
 //    mbarriers (waiting warps are suspended instead of polling shared memory).
 //  * Optionally (fused combine) the CTAs of one launch meet at a grid barrier once every split
@@ -74,8 +74,7 @@ constexpr int kMaxRP = 48;    // padded rows per KV head this kernel carries
 constexpr int kGroupRows = 16;
 constexpr int kKStages = 2;
 constexpr int kVStages = 3;
-constexpr int kSlices = kTile / 32;             // 32-key P slices of a tile (one per lane quadrant)
-constexpr int kSlicesPerStage = kVKeys / 32;    // slices a V stage's MMA step consumes
+constexpr int kSteps = kVKeys / 32;  // 32-key MMA steps of a V stage (one per lane quadrant)
 
 // K and V stages hold their 16-key chunks (one 4 KB page box each) back to back; inside a chunk,
 // [8-key group i][head-dim half h][key e][128 bytes] with the 128-byte swizzle, so the 8-key group
@@ -105,7 +104,7 @@ struct Cfg {
     static constexpr uint32_t kOffK = kOffQ + kQBytes;
     static constexpr uint32_t kOffV = kOffK + kKStages * kKStage;
     static constexpr uint32_t kOffP = kOffV + kVStages * kVStage;
-    static constexpr uint32_t kOffSmall = kOffP + kPStage;  // one P buffer, reused per slice
+    static constexpr uint32_t kOffSmall = kOffP + kPStage;  // one P buffer, reused per tile
     static constexpr uint32_t kColS = 0, kColO = SN;
     static constexpr uint32_t kTmemCols = 3 * SN <= 256 ? 256 : 512;
     static_assert(RP % kGroupRows == 0 && RP <= kMaxRP, "rows per CTA");
@@ -116,13 +115,14 @@ struct Cfg {
 
 struct Small {
     uint64_t kfull[kKStages], kempty[kKStages], sfull, sempty;
-    uint64_t pslice[kSlices];  // P slice q of the current tile written (one arrival per group)
+    uint64_t pfull;  // P of the current tile written (one arrival per softmax warp)
     uint64_t vfull[kVStages], vfree[kVStages], vtail;
     uint64_t odone, qready;
     uint64_t gbar[kMaxRP / kGroupRows];  // softmax group barriers (4 warp arrivals per phase)
     uint32_t tmem_base;
     int abort;
     int gvote[kMaxRP / kGroupRows][2][4];  // group votes: [group][phase parity][warp]
+    float vscale;  // v_scale, loaded while Q is staged (read after the last PV)
     alignas(16) float c0[kMaxRP];  // score scale of each row (log2 units per MMA unit), as float4
     float rmax[kMaxRP / kGroupRows][4][kGroupRows];  // per-group, per-warp row maxima of a tile
     float rsum[kMaxRP / kGroupRows][4][kGroupRows];  // per-group, per-warp row sums of the split
@@ -256,22 +256,19 @@ __device__ __forceinline__ int chunk_row(const PartialParams& p, const Small& sm
 }
 
 // The three term slices (columns base, base + RP, base + 2RP) of this lane's 16 rows, combined
-// as t0 + t1/16 + t2/256.
+// as t0 + t1/16 + t2/256 (the three loads in flight together, one wait).
 template <int RP>
 __device__ __forceinline__ void load_terms16(uint32_t taddr, float (&y)[kGroupRows]) {
-    uint32_t a[16];
-    tmem_ld16(taddr, a);
-    tmem_ld_wait(a);
+    uint32_t a0[16], a1[16], a2[16];
+    tmem_ld16(taddr, a0);
+    tmem_ld16(taddr + RP, a1);
+    tmem_ld16(taddr + 2 * RP, a2);
+    tmem_ld_wait(a0);
+    tmem_ld_wait(a1);
+    tmem_ld_wait(a2);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) y[i] = f32(a[i]);
-    tmem_ld16(taddr + RP, a);
-    tmem_ld_wait(a);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) y[i] = fmaf(f32(a[i]), 0.0625f, y[i]);
-    tmem_ld16(taddr + 2 * RP, a);
-    tmem_ld_wait(a);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) y[i] = fmaf(f32(a[i]), 0.00390625f, y[i]);
+    for (int i = 0; i < 16; ++i)
+        y[i] = fmaf(f32(a2[i]), 0.00390625f, fmaf(f32(a1[i]), 0.0625f, f32(a0[i])));
 }
 
 // Grid-wide barrier of one launch (thread 0 of every CTA) on a 64-bit ticket counter: CTA tickets
@@ -369,6 +366,10 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     // rows [row_lo, row_lo + R) of the slot: all of them unless R > 48 (row blocks)
     const RowBlock rblk = row_block(p);
     const int R = rblk.rows, row_lo = rblk.row_lo, G = p.group, P = p.page_size;
+    // With programmatic dependent launch the next kernel's CTAs may be scheduled from here on
+    // (onto SMs this grid leaves free); it waits for this grid's completion before it reads the
+    // workspace.
+    griddep_launch_dependents();
 
     // This CTA's workspace slot, and which (sequence, KV head) unit owns it, follow from every
     // context length (slots are shared out by length), a load away. For a batch of equal lengths
@@ -414,7 +415,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         }
         mbar_init(smem_u32(&sm.sfull), 1);
         mbar_init(smem_u32(&sm.sempty), C::kSoftWarps);
-        for (int i = 0; i < kSlices; ++i) mbar_init(smem_u32(&sm.pslice[i]), C::kGroups);
+        mbar_init(smem_u32(&sm.pfull), C::kSoftWarps);
         for (int i = 0; i < kVStages; ++i) {
             mbar_init(smem_u32(&sm.vfull[i]), 3);  // one arrival per copying warp
             mbar_init(smem_u32(&sm.vfree[i]), 1);
@@ -475,6 +476,11 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             }
         };
         const int kfirst = ci, vfirst = (ci + 1) % 3;
+        // Keys from n - q_len on (the drafted tokens) may be written by the kernel just before
+        // this one (their KV write): tiles reaching them are copied only after griddep_wait,
+        // which returns at once unless this grid is a programmatic dependent.
+        const int drafted = n - p.q_len;
+        bool dep_done = false;
         int krows[kOwn], vrows[kOwn];
         if (lane == 0) {
             own_rows(start, kfirst, krows);
@@ -497,6 +503,10 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             vready = __shfl_sync(0xffffffffu, vready, 0);
             if (kready) {
                 if (lane == 0) {
+                    if (!dep_done && start + (tk + 1) * kTile > drafted) {
+                        griddep_wait();
+                        dep_done = true;
+                    }
                     const int s = tk % kKStages;
                     const uint32_t bar = smem_u32(&sm.kfull[s]);
                     int nval = 0;
@@ -520,6 +530,10 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                 const int h0 = start + tv * kVKeys;
                 const int nkeys = min(kVKeys, end - h0);
                 uint8_t* vstage = smem + C::kOffV + vs * kVStage;
+                if (lane == 0 && !dep_done && h0 + kVKeys > drafted) {
+                    griddep_wait();
+                    dep_done = true;
+                }
                 if (nkeys == kVKeys) {
                     if (lane == 0) {
                         const uint32_t bar = smem_u32(&sm.vfull[vs]);
@@ -604,9 +618,12 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         // One thread, one event loop over two streams: QK of tile tq (its K copies landed and the
-        // softmax has read the previous scores) and PV of V stage up (its copies and the P slices
-        // it consumes are written). Polling both without blocking keeps a QK from queueing behind
-        // a PV whose V copies are late, and vice versa.
+        // softmax has read the previous scores) and PV of V stage up (its copies and the tile's
+        // probabilities are written). Polling both without blocking keeps a QK from queueing behind
+        // a PV whose V copies are late, and vice versa. When both are ready PV goes first: it
+        // frees the P buffer the softmax writes next and the V stage the next copy fills, while
+        // the scores of QK are needed only once the softmax is through the current tile (issuing
+        // eight MMAs blocks this thread while the tensor pipe drains the ones before them).
         if (lane == 0 && ctx.wait(&sm.qready, 0)) {
             const uint32_t idesc_qk = idesc_f32acc(128, SN, 0, 0, 0, 0);
             const uint32_t idesc_pv = idesc_f32acc(128, SN, 0, 0, 1, 1);
@@ -618,9 +635,41 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             uint32_t idle = 0;
             while (tq < ntiles || up < nvst) {
                 bool progressed = false;
-                if (tq < ntiles && mbar_test_wait(smem_u32(&sm.kfull[tq % kKStages]),
-                                                  (tq / kKStages) & 1) &&
-                    mbar_test_wait(smem_u32(&sm.sempty), (tq & 1) ^ 1)) {
+                if (up < nvst) {
+                    const int t = up / kStagesPerTile, hv = up % kStagesPerTile;
+                    const int vs = up % kVStages;
+                    // both tests issued back to back (no short circuit): their shared-memory
+                    // round trips overlap
+                    const bool ready =
+                        mbar_test_wait(smem_u32(&sm.vfull[vs]), (up / kVStages) & 1) &
+                        mbar_test_wait(smem_u32(&sm.pfull), t & 1);
+                    if (ready) {
+                        // O^T += V^T P^T over this stage's keys, both head-dim halves
+                        tc_fence_after();
+                        const uint32_t vb = smem_u32(smem + C::kOffV + vs * kVStage);
+#pragma unroll
+                        for (int kq = 0; kq < kSteps; ++kq) {
+                            const int kk = kSteps * hv + kq;  // 32-key step of the tile
+                            const uint64_t bd =
+                                smem_desc(pbase + kk * 512, 128, 2048, kSwizzleNone);
+#pragma unroll
+                            for (int dh = 0; dh < 2; ++dh) {
+                                // 32 keys = four 8-key groups from group 4 kq on
+                                const uint64_t ad =
+                                    smem_desc(vb + dh * kHalfOffset + kq * 4 * kGroupStride,
+                                              kVStage, kGroupStride, kSwizzle128B);
+                                mma_f8_ss(tmem + C::kColO + dh * SN, ad, bd, idesc_pv,
+                                          (t | kk) != 0);
+                            }
+                        }
+                        mma_commit(smem_u32(&sm.vfree[vs]));  // V stage and P buffer reusable
+                        ++up;
+                        progressed = true;
+                    }
+                }
+                if (tq < ntiles &&
+                    (mbar_test_wait(smem_u32(&sm.kfull[tq % kKStages]), (tq / kKStages) & 1) &
+                     mbar_test_wait(smem_u32(&sm.sempty), (tq & 1) ^ 1))) {
                     // S^T = K Q^T into the single S buffer
                     tc_fence_after();
                     const int s = tq % kKStages;
@@ -638,38 +687,6 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                     mma_commit(smem_u32(&sm.sfull));
                     ++tq;
                     progressed = true;
-                }
-                if (up < nvst) {
-                    const int t = up / kStagesPerTile, hv = up % kStagesPerTile;
-                    const int vs = up % kVStages;
-                    bool ready = mbar_test_wait(smem_u32(&sm.vfull[vs]), (up / kVStages) & 1);
-#pragma unroll
-                    for (int q = 0; q < kSlicesPerStage; ++q)
-                        ready = ready && mbar_test_wait(
-                                             smem_u32(&sm.pslice[kSlicesPerStage * hv + q]), t & 1);
-                    if (ready) {
-                        // O^T += V^T P^T over this stage's keys, both head-dim halves
-                        tc_fence_after();
-                        const uint32_t vb = smem_u32(smem + C::kOffV + vs * kVStage);
-#pragma unroll
-                        for (int kq = 0; kq < kSlicesPerStage; ++kq) {
-                            const int kk = kSlicesPerStage * hv + kq;  // 32-key step of the tile
-                            const uint64_t bd =
-                                smem_desc(pbase + kk * 512, 128, 2048, kSwizzleNone);
-#pragma unroll
-                            for (int dh = 0; dh < 2; ++dh) {
-                                // 32 keys = four 8-key groups from group 4 kq on
-                                const uint64_t ad =
-                                    smem_desc(vb + dh * kHalfOffset + kq * 4 * kGroupStride,
-                                              kVStage, kGroupStride, kSwizzle128B);
-                                mma_f8_ss(tmem + C::kColO + dh * SN, ad, bd, idesc_pv,
-                                          (t | kk) != 0);
-                            }
-                        }
-                        mma_commit(smem_u32(&sm.vfree[vs]));  // V stage and P slices reusable
-                        ++up;
-                        progressed = true;
-                    }
                 }
                 if (progressed) {
                     idle = 0;
@@ -695,10 +712,14 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
         const int qoff = n - p.q_len;  // row r of the slot sees keys j <= qoff + r / G
 
-        // Q -> three E4M3 terms (one warp per row), row scales
+        // Q -> three E4M3 terms (one warp per row), row scales. Q and the scales, and every
+        // workspace write below, come after the preceding kernel's completion (a no-op unless
+        // this grid is its programmatic dependent).
+        griddep_wait();
         {
             constexpr int kRowsPerWarp = RP / C::kSoftWarps;  // 4
             const float qk_scale = __ldg(p.k_scale) * 0.0625f * kLog2e;  // D^-1/2 = 1/16
+            if (sw == 0 && lane == 0) sm.vscale = __ldg(p.v_scale);  // seen by all after qready
             uint4 qraw[kRowsPerWarp];  // this warp's rows: all loads in flight at once
 #pragma unroll
             for (int k = 0; k < kRowsPerWarp; ++k) {
@@ -939,10 +960,10 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             make_p();
 #pragma unroll
             for (int q = 0; q < kGroupRows / 2; ++q) lsum[q] = add2(lsum[q], pv[q]);
-            // P slice wq (this warp's keys) is free once the V stage that consumed it in tile t-1
+            // this warp's keys of P are free once the V stage that consumed them in tile t-1
             // is done
             if (ok && t > 0) {
-                const int u = (kTile / kVKeys) * (t - 1) + wq / kSlicesPerStage;
+                const int u = (kTile / kVKeys) * (t - 1);
                 ok = ctx.wait_warp(&sm.vfree[u % kVStages], (u / kVStages) & 1);
             }
             if (!ok) {
@@ -957,7 +978,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             fence_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sm.pslice[wq]));
+            if (lane == 0) mbar_arrive(smem_u32(&sm.pfull));
         }
         // row sums over the 128 key lanes -> split state (max m - s, shifted sums and numerator)
 #pragma unroll
@@ -990,7 +1011,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         const bool ok = ctx.wait_warp(&sm.odone, 0);
         tc_fence_after();
         if (__all_sync(0xffffffffu, ok && !ctx.aborted())) {
-            const float vs = __ldg(p.v_scale);
+            const float vs = sm.vscale;
 #pragma unroll 1
             for (int dh = 0; dh < 2; ++dh) {
                 float o[kGroupRows];
@@ -1072,6 +1093,11 @@ static cudaError_t launch_rp(const CUtensorMap& kmap, const CUtensorMap& vmap,
     if (p.out) {  // the fused merge waits for every CTA: they must all be resident at once
         attr[0].id = cudaLaunchAttributeCooperative;
         attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    } else if (p.pdl) {  // a programmatic dependent of the preceding kernel on the stream
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
