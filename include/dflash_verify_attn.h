@@ -84,6 +84,17 @@ typedef enum {
 
 /* Bits of dflash_verify_attn_problem.flags. */
 #define DFLASH_PROBLEM_FUSED_COMBINE 0x1 /* forward merges the splits inside the partial launch */
+/* Launch the partial and combine kernels as programmatic dependents of the preceding kernel on
+ * the stream (CUDA programmatic dependent launch), so that each starts while its predecessor
+ * drains. A partial kernel then reads context_lens, the block table and the K/V pages of the
+ * positions before N - q_len while the preceding kernel may still be running; Q, k_scale,
+ * v_scale and the pages of the q_len drafted positions are read, and the split state in the
+ * workspace is written, only once it has completed (status flags are OR-ed into the status word
+ * at any time). The combine reads the workspace only once the partial kernel has completed. So set this bit only when the kernel launched just before run / forward writes none
+ * of context_lens, the block table or the pages of earlier positions (the drafted tokens' KV
+ * write, dflash_verify_attn_kv_write, writes only the drafted positions). Ignored with
+ * DFLASH_PROBLEM_FUSED_COMBINE. Results are the same bits with and without it. */
+#define DFLASH_PROBLEM_PDL 0x2
 
 /* Partial-attention kernel variants a plan can select. */
 #define DFLASH_KERNEL_AUTO 0

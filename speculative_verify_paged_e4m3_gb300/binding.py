@@ -25,6 +25,7 @@ DFLASH_FLAG_CONTEXT_CLAMPED = 0x1
 DFLASH_FLAG_CONTEXT_SHORT = 0x2
 DFLASH_FLAG_PAGE_CLAMPED = 0x4
 DFLASH_PROBLEM_FUSED_COMBINE = 0x1
+DFLASH_PROBLEM_PDL = 0x2
 DFLASH_KERNEL_AUTO = 0
 DFLASH_KERNEL_SIMT = 1
 DFLASH_KERNEL_TCGEN05 = 2

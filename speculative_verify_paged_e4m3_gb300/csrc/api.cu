@@ -110,6 +110,7 @@ PartialParams partial_params(const dflash_verify_attn_plan_t* plan, const void* 
     p.grid_bar = reinterpret_cast<unsigned long long*>(ws + kGridBarrierOffset);
     p.out = nullptr;  // partial state only; forward() sets these for a fused launch
     p.lse = nullptr;
+    p.pdl = (pr.flags & DFLASH_PROBLEM_PDL) && !plan->combine_fused ? 1 : 0;
     return p;
 }
 
@@ -395,6 +396,7 @@ int dflash_verify_attn_combine(const dflash_verify_attn_plan_t* plan, const void
     c.num_slots = plan->num_slots;
     c.tile_keys = plan->tile_keys;
     c.min_split_keys = plan->min_split_keys;
+    c.pdl = (pr.flags & DFLASH_PROBLEM_PDL) && !plan->combine_fused ? 1 : 0;
     if (launch_combine(c, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) {
         cudaGetLastError();
         return DFLASH_ERR_CUDA;
@@ -421,6 +423,7 @@ int dflash_verify_attn_forward(const dflash_verify_attn_plan_t* plan, const void
         if (workspace_bytes < plan->workspace_bytes) return DFLASH_ERR_WORKSPACE_TOO_SMALL;
         PartialParams p = partial_params(plan, q, k_pool, v_pool, block_table, context_lens,
                                          k_scale, v_scale, workspace);
+        p.pdl = 0;  // the cooperative fused launch is never a programmatic dependent
         p.out = static_cast<__half*>(out);
         p.lse = lse;
         if (launch_tc_partial(p, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) {

@@ -36,6 +36,7 @@ struct PartialParams {
     unsigned long long* grid_bar;  // ticket counter of the grid barrier (workspace header)
     __half* out;
     float* lse;
+    int pdl;  // host side: launch as a programmatic dependent of the preceding kernel
 };
 
 struct CombineParams {
@@ -47,6 +48,7 @@ struct CombineParams {
     int batch, q_len, num_q_heads, num_kv_heads, group, rows;
     int max_context, num_splits, tile_keys, min_split_keys;
     int num_slots;
+    int pdl;  // host side: launch as a programmatic dependent of the preceding kernel
 };
 
 // This CTA's place in a row-blocked grid: the split position x / row_blocks (the workspace slot
@@ -75,6 +77,19 @@ __device__ __forceinline__ RowBlock row_block(const PartialParams& p) {
     rb.slot = rb.xs + (gridDim.x / p.row_blocks) * (blockIdx.y + gridDim.y * blockIdx.z);
     return rb;
 }
+
+// ---- programmatic dependent launch -------------------------------------------------------------
+// Let the next kernel on the stream, if it was launched as this one's programmatic dependent,
+// start launching its CTAs (it still waits for this grid's completion where it calls
+// griddep_wait). Issued by every thread of a CTA; idempotent.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the grid this one depends on programmatically (the preceding kernel on the stream)
+// has completed and its memory writes are visible; returns at once when this grid was launched
+// without the programmatic attribute. The wait ends because that grid's CTAs are all resident
+// or done by the time this grid starts.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Context length of sequence b as the kernels see it: clamped into [0, max_context].
 __device__ __forceinline__ int clamped_context(const int32_t* context_lens, int b, int max_context,

@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(kSimtThreads, 1) simt_partial_kernel(PartialPa
     float* alpha_s = Ps + kSimtRows * kPStride;      // [kSimtRows]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    griddep_launch_dependents();  // the next kernel may start launching (programmatic launch)
     // this CTA's workspace slot and rows, and the (sequence, KV head) unit owning the slot
     // (slots are shared out by context length; common.cuh)
     const RowBlock rb = row_block(p);
@@ -62,6 +63,9 @@ __global__ void __launch_bounds__(kSimtThreads, 1) simt_partial_kernel(PartialPa
     const int start = split * per;
     if (start >= n) return;  // idle slot: the combine never reads it
     const int end = min(n, start + per);
+    // Q, the scales, the pages and the workspace only after the preceding kernel has completed
+    // (a no-op unless this grid is its programmatic dependent)
+    griddep_wait();
 
     const float qscale = __ldg(p.k_scale) * 0.0625f * kLog2e;  // D = 256: D^-1/2 = 1/16
     for (int idx = tid; idx < kSimtRows * kHeadDim; idx += kSimtThreads) {
@@ -180,8 +184,20 @@ cudaError_t launch_simt_partial(const PartialParams& p, cudaStream_t stream) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (!row_blocks_valid(p, kSimtRows)) return cudaErrorInvalidValue;
-    const dim3 grid = partial_grid(p);
-    simt_partial_kernel<<<grid, kSimtThreads, smem, stream>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = partial_grid(p);
+    cfg.blockDim = dim3(kSimtThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (p.pdl) {  // a programmatic dependent of the preceding kernel on the stream
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    e = cudaLaunchKernelEx(&cfg, simt_partial_kernel, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
