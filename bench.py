@@ -491,7 +491,7 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "f32" if plan.kernel == B.DFLASH_KERNEL_SIMT else "e4m3->f32",
         "data": "synthetic",
         "config": {
-            "workload": w.name, "layers": w.layers, "batch": w.batch, "q_len": w.q_len,
+            "workload": w.name, "layers": nl, "batch": w.batch, "q_len": w.q_len,
             "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
             "head_dim": w.head_dim, "context": list(w.context), "page_size": w.page_size,
             "kv_gb_per_step": round(w.kv_bytes_per_layer() * w.layers / 1e9, 4),

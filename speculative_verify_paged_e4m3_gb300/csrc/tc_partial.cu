@@ -55,6 +55,7 @@
 
 #include <cstddef>
 #include <mutex>
+#include <type_traits>
 
 #include "combine_impl.cuh"
 #include "common.cuh"
@@ -644,7 +645,8 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                         mbar_test_wait(smem_u32(&sm.vfull[vs]), (up / kVStages) & 1) &
                         mbar_test_wait(smem_u32(&sm.pfull), t & 1);
                     if (ready) {
-                        // O^T += V^T P^T over this stage's keys, both head-dim halves
+                        // O^T += V^T P^T over this stage's keys, both head-dim halves (the two
+                        // MMAs of a 32-key step back to back: they read the same P columns)
                         tc_fence_after();
                         const uint32_t vb = smem_u32(smem + C::kOffV + vs * kVStage);
 #pragma unroll
@@ -855,24 +857,38 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                 e[2 * i4] = add2(y[2 * i4], nm[2 * i4]);
                 e[2 * i4 + 1] = add2(y[2 * i4 + 1], nm[2 * i4 + 1]);
             }
+            // Every row of the group sees this key (all but the causal-window and ragged tiles):
+            // the per-row visibility tests are skipped below.
+            const bool all_rows = validm == 0xFFFFu;
+            if (all_rows) {
 #pragma unroll
-            for (int q = 0; q < kGroupRows / 2; ++q) {
-                need |= ((validm >> (2 * q)) & 1u) && lo2(e[q]) > kLazyThreshold;
-                need |= ((validm >> (2 * q + 1)) & 1u) && hi2(e[q]) > kLazyThreshold;
+                for (int q = 0; q < kGroupRows / 2; ++q)
+                    need |= (lo2(e[q]) > kLazyThreshold) | (hi2(e[q]) > kLazyThreshold);
+            } else {
+#pragma unroll
+                for (int q = 0; q < kGroupRows / 2; ++q) {
+                    need |= ((validm >> (2 * q)) & 1u) && lo2(e[q]) > kLazyThreshold;
+                    need |= ((validm >> (2 * q + 1)) & 1u) && hi2(e[q]) > kLazyThreshold;
+                }
             }
             // shifted probabilities -> three E4M3 terms (this thread's 16 rows of each term are one
             // 16-byte chunk of P); row sums take the unrounded values
             uint64_t pv[kGroupRows / 2];
             uint32_t code[kTerms][4];
-            auto make_p = [&]() {
+            // kAll: every row visible (no per-row tests)
+            auto make_p = [&](auto all) {
+                constexpr bool kAll = decltype(all)::value;
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
                     uint32_t ch[2], cm[2], cl[2];
 #pragma unroll
                     for (int q = 0; q < 2; ++q) {
                         const int jj = 2 * w + q;
-                        const float p0 = ((validm >> (2 * jj)) & 1u) ? ex2(lo2(e[jj])) : 0.f;
-                        const float p1 = ((validm >> (2 * jj + 1)) & 1u) ? ex2(hi2(e[jj])) : 0.f;
+                        const float p0 = (kAll || ((validm >> (2 * jj)) & 1u)) ? ex2(lo2(e[jj]))
+                                                                               : 0.f;
+                        const float p1 = (kAll || ((validm >> (2 * jj + 1)) & 1u))
+                                             ? ex2(hi2(e[jj]))
+                                             : 0.f;
                         pv[jj] = pk2(p0, p1);
                         // h, m: truncations to 4 significant bits (mantissa masked), so p - h and
                         // r - m are exact and the three terms sum to p up to l's final rounding
@@ -957,7 +973,10 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                     }
                 }
             }
-            make_p();
+            if (all_rows)
+                make_p(std::true_type{});
+            else
+                make_p(std::false_type{});
 #pragma unroll
             for (int q = 0; q < kGroupRows / 2; ++q) lsum[q] = add2(lsum[q], pv[q]);
             // this warp's keys of P are free once the V stage that consumed them in tile t-1
