@@ -30,15 +30,18 @@
 //    2^(8 - s) (then the warpgroup rescales its O columns in tensor memory), and FP32 row sums of
 //    the unrounded (shifted) probabilities, reduced across the key lanes once per split. The
 //    split state keeps m - s as its max, which makes the shift invisible to the combine.
-//  * Warp roles: warps 0 and 3 copy K tiles (TMA, 2 stages of 128 keys, half of each tile's
-//    chunks each); warp 2 copies V (TMA, 3 stages of 128 keys) and zeroes the keys past the
-//    context in the last one (a zero probability must not meet a NaN code); warp 1 owns tensor
-//    memory and issues the MMAs from one thread that polls both streams (QK of the next tile, PV
-//    of the next V stage) without blocking on either; warps 4.. stage the Q terms (while the first
-//    copies are in flight), then run the softmax and write O out. The copies come from three
-//    warps: on this GPU the copy throughput of one SM grows with the number of warps issuing them
-//    (measured with this very box pattern: 4.4, 6.2 and 6.6 TB/s over the whole GPU for one, two
-//    and three warps).
+//  * Warp roles: warps 0, 2 and 3 share the copies of K (TMA, 3 stages of 128 keys) and V (2
+//    stages), each a fixed third of every tile's 16-key page chunks; the last ragged V stage is
+//    copied whole by one of them, which zeroes its keys past the context (a zero probability must
+//    not meet a NaN code). Three K stages against two V stages: the K ring (a copy lands about
+//    1.5 us after it is issued, and tile t+3's copy waits for QK of tile t) binds the tile period,
+//    while V of a tile is needed only after its softmax. Warp 1 owns tensor memory and issues the
+//    MMAs from one thread that polls both streams (QK of the next tile, PV of the next V stage)
+//    without blocking on either; warps 4.. stage the Q terms (while the first copies are in
+//    flight), then run the softmax and write O out. The copies come from three warps: on this
+//    GPU the copy throughput of one SM grows with the number of warps issuing them (measured with
+//    this very box pattern: 4.4, 6.2 and 6.6 TB/s over the whole GPU for one, two and three
+//    warps).
 //  * One P buffer: the softmax warp of lane quadrant q writes keys [32q, 32q + 32) of every
 //    tile once the PV of the previous tile has read them; the PV of a tile waits for one
 //    barrier that every softmax warp arrives on (one test for the MMA thread to poll).
@@ -73,8 +76,8 @@ constexpr int kVKeys = 128;   // keys per V stage (a whole tile: four 32-key MMA
 constexpr int kTerms = 3;     // E4M3 terms of Q and of P
 constexpr int kMaxRP = 48;    // padded rows per KV head this kernel carries
 constexpr int kGroupRows = 16;
-constexpr int kKStages = 2;
-constexpr int kVStages = 3;
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
 constexpr int kSteps = kVKeys / 32;  // 32-key MMA steps of a V stage (one per lane quadrant)
 
 // K and V stages hold their 16-key chunks (one 4 KB page box each) back to back; inside a chunk,
@@ -127,6 +130,7 @@ struct Small {
     alignas(16) float c0[kMaxRP];  // score scale of each row (log2 units per MMA unit), as float4
     float rmax[kMaxRP / kGroupRows][4][kGroupRows];  // per-group, per-warp row maxima of a tile
     float rsum[kMaxRP / kGroupRows][4][kGroupRows];  // per-group, per-warp row sums of the split
+    float mref[kMaxRP / kGroupRows][kGroupRows];     // the split state's max (m - s) of each row
     int rows[kRowCache];  // source row (physical page * page + slot) of chunk c of the split
 };
 static_assert(offsetof(Small, c0) % 16 == 0, "row constants are read as float4");
@@ -1006,24 +1010,20 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             if (lane == 0) {
                 sm.rsum[g][wq][2 * q] = v0;
                 sm.rsum[g][wq][2 * q + 1] = v1;
+                if (wq == 0) {
+                    sm.mref[g][2 * q] = -lo2(nm[q]);
+                    sm.mref[g][2 * q + 1] = -hi2(nm[q]);
+                }
             }
         }
         if (alive) alive = group_sync(ctx, g, wq, epoch, false, nullptr);
         const int64_t unit = slot;  // this split's workspace slot
-        if (alive && !ctx.aborted()) {
-#pragma unroll
-            for (int q = 0; q < kGroupRows / 2; ++q) {
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int i = 2 * q + k;
-                    if (st == i && row0 + i < R) {
-                        const float L = sm.rsum[g][0][i] + sm.rsum[g][1][i] + sm.rsum[g][2][i] +
-                                        sm.rsum[g][3][i];
-                        p.ws_state[unit * p.rows + row_lo + row0 + i] =
-                            make_float2(-(k ? hi2(nm[q]) : lo2(nm[q])), L);
-                    }
-                }
-            }
+        // lane i of the group's first warp writes row i (a compact block: this code runs once per
+        // CTA, from a cold instruction cache)
+        if (alive && !ctx.aborted() && wq == 0 && lane < kGroupRows && row0 + lane < R) {
+            const float L = sm.rsum[g][0][lane] + sm.rsum[g][1][lane] + sm.rsum[g][2][lane] +
+                            sm.rsum[g][3][lane];
+            p.ws_state[unit * p.rows + row_lo + row0 + lane] = make_float2(sm.mref[g][lane], L);
         }
         // O^T (tensor memory, lane = head-dim element) -> numerator rows:
         // O = O_h + O_m/16 + O_l/256
