@@ -164,11 +164,6 @@ __device__ __forceinline__ float warp_max(float v) {
     asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
     return r;
 }
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
 
 // Bounded wait on an mbarrier phase (try_wait lets the hardware suspend the thread meanwhile):
 // gives up when the CTA's abort flag is raised or after kWaitLimitNs.
@@ -1003,14 +998,32 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sm.pfull));
         }
-        // row sums over the 128 key lanes -> split state (max m - s, shifted sums and numerator)
+        // row sums over the 128 key lanes -> split state (max m - s, shifted sums and numerator).
+        // A transposed butterfly over the warp: each step trades half of the rows with the lane
+        // `off` away, so lane l ends with row (l >> 1) & 15 after 16 shuffles, each sum taken in
+        // the order of a plain xor reduction of that row (same bits, far less code).
+        {
+            float v[kGroupRows];
 #pragma unroll
-        for (int q = 0; q < kGroupRows / 2; ++q) {
-            const float v0 = warp_sum(lo2(lsum[q])), v1 = warp_sum(hi2(lsum[q]));
-            if (lane == 0) {
-                sm.rsum[g][wq][2 * q] = v0;
-                sm.rsum[g][wq][2 * q + 1] = v1;
-                if (wq == 0) {
+            for (int q = 0; q < kGroupRows / 2; ++q) {
+                v[2 * q] = lo2(lsum[q]);
+                v[2 * q + 1] = hi2(lsum[q]);
+            }
+#pragma unroll
+            for (int half = kGroupRows / 2, off = 16; half >= 1; half >>= 1, off >>= 1) {
+                const bool upper = (lane & off) != 0;
+#pragma unroll
+                for (int j = 0; j < half; ++j) {
+                    const float keep = upper ? v[j + half] : v[j];
+                    const float send = upper ? v[j] : v[j + half];
+                    v[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                }
+            }
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+            if ((lane & 1) == 0) sm.rsum[g][wq][lane >> 1] = v[0];
+            if (lane == 0 && wq == 0) {
+#pragma unroll
+                for (int q = 0; q < kGroupRows / 2; ++q) {
                     sm.mref[g][2 * q] = -lo2(nm[q]);
                     sm.mref[g][2 * q + 1] = -hi2(nm[q]);
                 }
