@@ -131,6 +131,7 @@ struct Small {
     float rmax[kMaxRP / kGroupRows][4][kGroupRows];  // per-group, per-warp row maxima of a tile
     float rsum[kMaxRP / kGroupRows][4][kGroupRows];  // per-group, per-warp row sums of the split
     float mref[kMaxRP / kGroupRows][kGroupRows];     // the split state's max (m - s) of each row
+    float nmcur[kMaxRP / kGroupRows][4][kGroupRows];  // each warp's copy of s - reference max
     int rows[kRowCache];  // source row (physical page * page + slot) of chunk c of the split
 };
 static_assert(offsetof(Small, c0) % 16 == 0, "row constants are read as float4");
@@ -234,9 +235,9 @@ __device__ __forceinline__ bool group_sync(const Ctx& ctx, int g, int wq, int& e
     return group_wait(ctx, g, group_arrive(ctx, g, wq, epoch, vote), any);
 }
 
-// (pool row, clamped?) of key j0 of sequence b from the block table (splits longer than the
-// row cache: inline, so that a copier's lookups for one stage are all in flight together)
-__device__ __forceinline__ int2 table_row(const int32_t* block_table, int b, int max_pages_per_seq,
+// (pool row, clamped?) of key j0 of sequence b from the block table, for splits longer than the
+// row cache (out of line: the copiers' common path stays compact)
+__device__ __noinline__ int2 table_row(const int32_t* block_table, int b, int max_pages_per_seq,
                                        int page_size, int num_pages, int j0) {
     bool clamped = false;
     const int phys = physical_page(block_table, b, max_pages_per_seq, j0 / page_size, num_pages,
@@ -803,6 +804,8 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         uint64_t nm[kGroupRows / 2];
 #pragma unroll
         for (int q = 0; q < kGroupRows / 2; ++q) nm[q] = pk2(INFINITY, INFINITY);
+        if (lane < kGroupRows) sm.nmcur[g][wq][lane] = INFINITY;
+        __syncwarp();
         const uint64_t k16th = pk2(0.0625f, 0.0625f), k256th = pk2(0.00390625f, 0.00390625f);
         const uint64_t k16 = pk2(16.f, 16.f);
         constexpr uint64_t kTrunc4 = 0xFFF00000FFF00000ull;  // sign, exponent, 3 mantissa bits
@@ -913,37 +916,51 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             }
             bool ok = true;
             if (need_any) {
-                // exact tile maximum per row -> new reference max (every thread of the group
-                // derives the same values from the warps' partial maxima); rescale row sums and O
+                // exact tile maximum per row -> new reference max; rescale row sums and O. The
+                // warp's row maxima by a transposed butterfly (lane l ends with row (l >> 1) & 15),
+                // the group's through shared memory; lanes 2i and 2i + 1 then derive row i's new
+                // reference and weight, which the shuffles below hand to every lane (compact code:
+                // tile 0 runs it cold, later tiles rarely)
+                {
+                    float v[kGroupRows];
 #pragma unroll
-                for (int q = 0; q < kGroupRows / 2; ++q) {
-                    const float m0 = warp_max(((validm >> (2 * q)) & 1u) ? lo2(y[q]) : -INFINITY);
-                    const float m1 =
-                        warp_max(((validm >> (2 * q + 1)) & 1u) ? hi2(y[q]) : -INFINITY);
-                    if (lane == 0) {
-                        sm.rmax[g][wq][2 * q] = m0;
-                        sm.rmax[g][wq][2 * q + 1] = m1;
+                    for (int q = 0; q < kGroupRows / 2; ++q) {
+                        v[2 * q] = ((validm >> (2 * q)) & 1u) ? lo2(y[q]) : -INFINITY;
+                        v[2 * q + 1] = ((validm >> (2 * q + 1)) & 1u) ? hi2(y[q]) : -INFINITY;
                     }
+#pragma unroll
+                    for (int half = kGroupRows / 2, off = 16; half >= 1; half >>= 1, off >>= 1) {
+                        const bool upper = (lane & off) != 0;
+#pragma unroll
+                        for (int j = 0; j < half; ++j) {
+                            const float keep = upper ? v[j + half] : v[j];
+                            const float send = upper ? v[j] : v[j + half];
+                            v[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, off));
+                        }
+                    }
+                    v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
+                    if ((lane & 1) == 0) sm.rmax[g][wq][lane >> 1] = v[0];
                 }
                 if (!group_sync(ctx, g, wq, epoch, false, nullptr)) {
                     alive = false;
                     break;
                 }
+                const int ri = (lane >> 1) & (kGroupRows - 1);
+                const float mo = kPShift - sm.nmcur[g][wq][ri];
+                const float tm = fmaxf(fmaxf(sm.rmax[g][0][ri], sm.rmax[g][1][ri]),
+                                       fmaxf(sm.rmax[g][2][ri], sm.rmax[g][3][ri]));
+                const float mn = fmaxf(mo, tm);
+                const float alpha_r = (mn == -INFINITY) ? 1.f : ex2(mo - mn);
+                const float nm_r = (mn == -INFINITY) ? INFINITY : kPShift - mn;
+                __syncwarp();  // every lane has read its row's old reference
+                if ((lane & 1) == 0) sm.nmcur[g][wq][ri] = nm_r;
                 float alpha[kGroupRows];
 #pragma unroll
                 for (int q = 0; q < kGroupRows / 2; ++q) {
-                    float nmq[2] = {lo2(nm[q]), hi2(nm[q])};
-#pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const int i = 2 * q + k;
-                        const float mo = kPShift - nmq[k];
-                        const float tm = fmaxf(fmaxf(sm.rmax[g][0][i], sm.rmax[g][1][i]),
-                                               fmaxf(sm.rmax[g][2][i], sm.rmax[g][3][i]));
-                        const float mn = fmaxf(mo, tm);
-                        alpha[i] = (mn == -INFINITY) ? 1.f : ex2(mo - mn);
-                        nmq[k] = (mn == -INFINITY) ? INFINITY : kPShift - mn;
-                    }
-                    nm[q] = pk2(nmq[0], nmq[1]);
+                    alpha[2 * q] = __shfl_sync(0xffffffffu, alpha_r, 4 * q);
+                    alpha[2 * q + 1] = __shfl_sync(0xffffffffu, alpha_r, 4 * q + 2);
+                    nm[q] = pk2(__shfl_sync(0xffffffffu, nm_r, 4 * q),
+                                __shfl_sync(0xffffffffu, nm_r, 4 * q + 2));
                     lsum[q] = mul2(lsum[q], pk2(alpha[2 * q], alpha[2 * q + 1]));
                     e[q] = add2(y[q], nm[q]);
                 }
