@@ -66,6 +66,10 @@ int check_plan(const dflash_verify_attn_plan_t* plan) {
     if (plan->problem.batch == 1 ? plan->num_slots != units * plan->num_splits
                                  : plan->num_slots < units)
         return DFLASH_ERR_INVALID_ARGUMENT;
+    // the kernels' tile sizes are compile-time constants: split boundaries fall on their tiles
+    if (plan->tile_keys != (plan->kernel == DFLASH_KERNEL_TCGEN05 ? 128 : 32) ||
+        plan->min_split_keys % plan->tile_keys != 0)
+        return DFLASH_ERR_INVALID_ARGUMENT;
     // every row block holds 1..capacity rows of the plan's kernel
     const int64_t block_rows = ceil_div(plan->rows, plan->row_blocks);
     const int capacity = plan->kernel == DFLASH_KERNEL_TCGEN05 ? tc_max_rows() : simt_max_rows();
@@ -111,6 +115,10 @@ PartialParams partial_params(const dflash_verify_attn_plan_t* plan, const void* 
     p.out = nullptr;  // partial state only; forward() sets these for a fused launch
     p.lse = nullptr;
     p.pdl = (pr.flags & DFLASH_PROBLEM_PDL) && !plan->combine_fused ? 1 : 0;
+    p.per_max = host_keys_per_split(pr.max_context, plan);
+    p.page_shift = -1;
+    for (int s = 0; s < 31; ++s)
+        if (pr.page_size == (1 << s)) p.page_shift = s;
     return p;
 }
 

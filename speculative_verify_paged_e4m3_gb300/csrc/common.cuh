@@ -31,6 +31,9 @@ struct PartialParams {
     // Row blocks: the grid's x extent is num_splits * row_blocks; CTA x = split * row_blocks + k
     // carries rows [k * block_rows, min(rows, (k + 1) * block_rows)) of that split's slot.
     int row_blocks, block_rows;
+    // keys per split of a max_context-long context (the split size the kernels guess while the
+    // context length is in flight), and log2 of page_size when it is a power of two (else -1)
+    int per_max, page_shift;
     // merge of the splits inside the same launch (every CTA resident): grid barrier words in the
     // workspace header, then FP16 output and FP32 log-sum-exp; null out when not fused
     unsigned long long* grid_bar;  // ticket counter of the grid barrier (workspace header)
@@ -71,6 +74,13 @@ inline bool row_blocks_valid(const PartialParams& p, int capacity) {
 
 __device__ __forceinline__ RowBlock row_block(const PartialParams& p) {
     RowBlock rb;
+    if (p.row_blocks == 1) {  // one CTA per split: no division
+        rb.xs = blockIdx.x;
+        rb.row_lo = 0;
+        rb.rows = p.rows;
+        rb.slot = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+        return rb;
+    }
     rb.xs = blockIdx.x / p.row_blocks;
     rb.row_lo = (blockIdx.x - rb.xs * p.row_blocks) * p.block_rows;
     rb.rows = min(p.block_rows, p.rows - rb.row_lo);

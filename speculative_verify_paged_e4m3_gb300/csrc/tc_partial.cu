@@ -379,17 +379,29 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
     // (split sizes are whole tiles, so any context close to max_context): thread c looks up
     // chunk c of that range while the lengths are in flight, and the row cache below takes it if
     // the guess holds.
-    const int per_max = keys_per_split(p.max_context, p.num_splits, p.tile_keys, p.min_split_keys);
+    // (divisions by the page size become shifts for power-of-two pages, and the tile size is
+    // this kernel's constant: the set-up's dependent chain is short)
+    const int per_max = p.per_max;
     int page_max = 0;
-    if (tid < kRowCache && rblk.xs * per_max + tid * kChunk < p.max_context)
+    if (tid < kRowCache && rblk.xs * per_max + tid * kChunk < p.max_context) {
+        const int j = rblk.xs * per_max + tid * kChunk;
         page_max = p.block_table[(int64_t)blockIdx.z * p.max_pages_per_seq +
-                                 (rblk.xs * per_max + tid * kChunk) / P];
+                                 (p.page_shift >= 0 ? j >> p.page_shift : j / P)];
+    }
     const int slot = rblk.slot;
-    const UnitSlots us = locate_slots(p.context_lens, p.batch, p.num_kv_heads, p.num_splits,
-                                      p.num_slots, p.max_context, p.q_len, slot, true);
+    // a single sequence's unit is the grid row (KV head): no search, no division
+    const UnitSlots us =
+        p.batch == 1 ? locate_slots_single(p.context_lens, p.num_kv_heads, p.num_splits,
+                                           p.max_context, p.q_len, blockIdx.y, false)
+                     : locate_slots(p.context_lens, p.batch, p.num_kv_heads, p.num_splits,
+                                    p.num_slots, p.max_context, p.q_len, slot, true);
     if (slot == 0 && tid == 0 && us.flags) atomicOr(p.status, us.flags);
     const int b = us.b, h = us.h, split = slot - us.first, n = us.n;
-    const int per = b >= 0 ? keys_per_split(n, us.count, p.tile_keys, p.min_split_keys) : 1;
+    int per = 1;
+    if (b >= 0) {  // keys_per_split with this kernel's tile size
+        per = max((n + us.count - 1) / us.count, p.min_split_keys);
+        per = (per + kTile - 1) / kTile * kTile;
+    }
     const int start = split * per;
     if (b < 0 || start >= n) {  // idle slot: the combine never reads it
         if constexpr (kFused) fused_merge<C::kThreads>(p, smem);
@@ -438,11 +450,12 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         const int nchunks = min((end - start + kChunk - 1) / kChunk, kRowCache);
         for (int c = tid; c < nchunks; c += C::kThreads) {
             const int j0 = start + c * kChunk;
+            const int lp = p.page_shift >= 0 ? j0 >> p.page_shift : j0 / P;
             const int phys = (guessed && c == tid)
                                  ? clamp_page(page_max, p.num_pages, &clamped)
-                                 : physical_page(p.block_table, b, p.max_pages_per_seq, j0 / P,
+                                 : physical_page(p.block_table, b, p.max_pages_per_seq, lp,
                                                  p.num_pages, &clamped);
-            sm.rows[c] = phys * P + (j0 % P);
+            sm.rows[c] = phys * P + (j0 - lp * P);
         }
         if (clamped) atomicOr(p.status, DFLASH_FLAG_PAGE_CLAMPED);
     }

@@ -149,6 +149,19 @@ def test_plan_row_blocks_tampered(B, row_blocks):
     assert e.value.status == B.DFLASH_ERR_INVALID_ARGUMENT
 
 
+@pytest.mark.parametrize("kernel,tile,min_keys", [
+    ("tc", 64, 256), ("tc", 256, 256), ("tc", 128, 200), ("simt", 128, 256), ("simt", 32, 48)])
+def test_plan_tile_keys_tampered(B, kernel, tile, min_keys):
+    # the kernels' tiles are compile-time constants (128 keys tensor-core, 32 CUDA-core): a plan
+    # that says otherwise, or whose minimum split is not whole tiles, is refused
+    kw = {} if kernel == "tc" else {"kernel": B.DFLASH_KERNEL_SIMT}
+    plan = B.dflash_verify_attn_plan(problem(B, **kw))
+    plan.tile_keys, plan.min_split_keys = tile, min_keys
+    with pytest.raises(B.DflashError) as e:
+        B.dflash_verify_attn_split_slots(plan, [1000])
+    assert e.value.status == B.DFLASH_ERR_INVALID_ARGUMENT
+
+
 @pytest.mark.parametrize("batch,hkv,q_len,splits,fused,slots", [
     (1, 1, 8, 0, False, 152),      # one sequence: Hkv * num_splits
     (1, 4, 8, 0, False, 152),
