@@ -1,7 +1,10 @@
 """Benchmark: 16-layer q8 verification attention over a paged E4M3 KV cache on one GB300.
 
 A step is one pass of the whole path (16 layers x [partial attention + combine]) over the
-workload's resident inputs, replayed from one CUDA graph. Default workload: 16 layers, batch 1,
+workload's resident inputs, replayed from one CUDA graph; each kernel is launched as a programmatic
+dependent of the kernel before it (it starts while that one drains and waits for it before reading
+Q or writing anything; `--pdl off`: plain stream order, which the line also reports). Default
+workload: 16 layers, batch 1,
 q_len 8, Hq 6, Hkv 1, D 256, context 261888 (the capacity boundary window), page 16, shuffled
 block tables, 2.15 GB of distinct E4M3 K/V per step (far larger than L2, so no flush is needed;
 smaller workloads get a 512 MB L2 flush between timed steps).
@@ -49,8 +52,9 @@ def parse_args():
                     help="time only the first L layers (profiling captures; 0: all)")
     ap.add_argument("--fused-combine", action="store_true",
                     help="merge the splits inside the partial launch (one kernel per layer)")
-    ap.add_argument("--pdl", choices=["on", "off"], default="off",
-                    help="launch the kernels as programmatic dependents of the preceding kernel")
+    ap.add_argument("--pdl", choices=["on", "off"], default="on",
+                    help="launch the kernels as programmatic dependents of the preceding kernel "
+                         "(on: the step line also reports the same step in plain stream order)")
     ap.add_argument("--l2", choices=["auto", "warm"], default="auto",
                     help="auto: flush L2 (512 MB write) between timed steps when the workload's "
                          "KV is under 4x L2; warm: never flush (cache-resident small workloads)")
@@ -345,6 +349,17 @@ def run_ours(args, rank, world, local_rank):
         partial_ms = timed_replays(g_partial)
         combine_ms = timed_replays(g_combine)
 
+    # with programmatic launch, the same step in plain stream order (same layers, workspace and
+    # split plan; only the launch flag differs), for comparison
+    stream_order = None
+    if args.pdl == "on" and not fused:
+        plain = B.Plan.from_buffer_copy(plan)
+        plain.problem.flags = plan.problem.flags & ~B.DFLASH_PROBLEM_PDL
+        g_plain = stack._capture(lambda: stack.launch(plan=plain))
+        so_ms = max_over_ranks(timed_replays(g_plain) * nl, world, dev)
+        stream_order = {"ms_per_step": round(so_ms, 4),
+                        "frac_of_measured": None}  # filled in below, once the peak is known
+
     # end to end through the public API: per step, H2D of the step's inputs from pinned host
     # memory (Q, block tables, context lengths, scales of all layers), the 16 layers, and D2H of
     # the outputs and LSEs; the KV cache stays resident (it is the model's state, not an input)
@@ -460,6 +475,9 @@ def run_ours(args, rank, world, local_rank):
         "target_frac": TARGET_FRAC,
         "target_ms_at_measured_peak": round(step_bytes / (TARGET_FRAC * peak * 1e9) * 1e3, 4),
     }
+    if stream_order is not None:
+        stream_order["frac_of_measured"] = round(
+            step_bytes / (stream_order["ms_per_step"] * 1e-3) / 1e9 / peak, 4)
     kernel_bytes_ws_free = nbytes["kv"] + nbytes["bt"] + nbytes["q"]
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -515,6 +533,7 @@ def run_ours(args, rank, world, local_rank):
                 kernel_bytes_ws_free / (partial_ms * 1e-3) / 1e9 / peak, 4)),
         },
         "step_roofline": step_roofline,
+        "step_in_stream_order": stream_order,
         "step_hbm_gbs": round(step_gbs, 1),
         "step_frac_of_peak": round(step_gbs / peak, 4),
         "combine_kernel_ms": round(combine_ms, 5),

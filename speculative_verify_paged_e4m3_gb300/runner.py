@@ -55,10 +55,12 @@ class LayerStack:
     def plan(self):
         return self.att.plan
 
-    def launch(self, stream=None):
-        """16 x (partial attention + combine), enqueued on the stream."""
+    def launch(self, stream=None, plan=None):
+        """16 x (partial attention + combine), enqueued on the stream (with another plan of the
+        same shapes, e.g. other launch flags, when given)."""
+        plan = self.plan if plan is None else plan
         for lay, out, lse in zip(self.layers, self.outs, self.lses):
-            B.dflash_verify_attn_forward(self.plan, lay["q"], lay["k_pool"], lay["v_pool"],
+            B.dflash_verify_attn_forward(plan, lay["q"], lay["k_pool"], lay["v_pool"],
                                          lay["block_table"], lay["context_lens"], lay["k_scale"],
                                          lay["v_scale"], self.att.workspace, out, lse, stream)
 

@@ -1,6 +1,7 @@
 """Full-size workloads in the launch configuration the benchmark times (16 layers, each with its
-own KV allocation, captured in one CUDA graph and replayed), checked against the oracle on
-sampled layers (the first and the last: every row of those layers, element by element)."""
+own KV allocation, launched as programmatic dependents, captured in one CUDA graph and replayed),
+checked against the oracle on sampled layers (the first and the last: every row of those layers,
+element by element)."""
 import gc
 
 import pytest
@@ -26,8 +27,9 @@ def built():
 
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
 def test_full_size_graph_replay_sampled_layers(w):
+    from speculative_verify_paged_e4m3_gb300 import binding as B
     from speculative_verify_paged_e4m3_gb300.runner import LayerStack
-    stack = LayerStack(w, device="cuda")
+    stack = LayerStack(w, device="cuda", flags=B.DFLASH_PROBLEM_PDL)
     try:
         stack.capture()
         stack.replay()
