@@ -90,9 +90,10 @@ typedef enum {
  * positions before N - q_len while the preceding kernel may still be running; Q, k_scale,
  * v_scale and the pages of the q_len drafted positions are read, and the split state in the
  * workspace is written, only once it has completed (status flags are OR-ed into the status word
- * at any time). The combine reads the workspace only once the partial kernel has completed. So set this bit only when the kernel launched just before run / forward writes none
- * of context_lens, the block table or the pages of earlier positions (the drafted tokens' KV
- * write, dflash_verify_attn_kv_write, writes only the drafted positions). Ignored with
+ * at any time). The combine reads the workspace only once the partial kernel has completed.
+ * So set this bit only when the kernel launched just before run / forward writes none of
+ * context_lens, the block table or the pages of earlier positions (the drafted tokens' KV write,
+ * dflash_verify_attn_kv_write, writes only the drafted positions). Ignored with
  * DFLASH_PROBLEM_FUSED_COMBINE. Results are the same bits with and without it. */
 #define DFLASH_PROBLEM_PDL 0x2
 
