@@ -503,6 +503,8 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms, 4),
+        "step_ms_median": round(statistics.median(step_ms), 4),
+        "step_ms_min": round(min(step_ms), 4),
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,
