@@ -24,6 +24,7 @@ DFLASH_ERR_CUDA = -4
 DFLASH_FLAG_CONTEXT_CLAMPED = 0x1
 DFLASH_FLAG_CONTEXT_SHORT = 0x2
 DFLASH_FLAG_PAGE_CLAMPED = 0x4
+DFLASH_FLAG_KERNEL_TIMEOUT = 0x8
 DFLASH_PROBLEM_FUSED_COMBINE = 0x1
 DFLASH_PROBLEM_PDL = 0x2
 DFLASH_KERNEL_AUTO = 0
