@@ -45,12 +45,15 @@
 //  * One P buffer: the softmax warp of lane quadrant q writes keys [32q, 32q + 32) of every
 //    tile once the PV of the previous tile has read them; the PV of a tile waits for one
 //    barrier that every softmax warp arrives on (one test for the MMA thread to poll).
-//  * The softmax math runs on FP32 pairs (f32x2 instructions), the warpgroup barriers on
-//    mbarriers (waiting warps are suspended instead of polling shared memory).
+//  * The softmax math runs on FP32 pairs (f32x2 instructions). A warpgroup synchronises on a
+//    hardware named barrier (one per group), whose reduction also carries the vote on moving the
+//    reference max.
 //  * Optionally (fused combine) the CTAs of one launch meet at a grid barrier once every split
 //    state is written and merge the splits themselves.
-//    Every wait is bounded: on timeout the CTA sets DFLASH_FLAG_KERNEL_TIMEOUT, drains its copies
-//    and returns.
+//    Every wait on another warp's or the copy engine's progress is bounded: on timeout the CTA
+//    sets DFLASH_FLAG_KERNEL_TIMEOUT, drains its copies and returns. A softmax warp whose wait
+//    gave up still runs the rest of its tiles without work, so the four warps of a group always
+//    reach the same named barriers.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -122,10 +125,8 @@ struct Small {
     uint64_t pfull;  // P of the current tile written (one arrival per softmax warp)
     uint64_t vfull[kVStages], vfree[kVStages], vtail;
     uint64_t odone, qready;
-    uint64_t gbar[kMaxRP / kGroupRows];  // softmax group barriers (4 warp arrivals per phase)
     uint32_t tmem_base;
     int abort;
-    int gvote[kMaxRP / kGroupRows][2][4];  // group votes: [group][phase parity][warp]
     float vscale;  // v_scale, loaded while Q is staged (read after the last PV)
     alignas(16) float c0[kMaxRP];  // score scale of each row (log2 units per MMA unit), as float4
     float rmax[kMaxRP / kGroupRows][4][kGroupRows];  // per-group, per-warp row maxima of a tile
@@ -207,32 +208,23 @@ struct Ctx {
     __device__ bool aborted() const { return *reinterpret_cast<volatile int*>(&sm->abort) != 0; }
 };
 
-// Barrier of one softmax warpgroup (4 warps) on its mbarrier, in two halves so that work can go
-// on between them: group_arrive publishes this warp's vote (lane 0 stores it and arrives, with
-// release semantics) and returns the barrier phase; group_wait waits for that phase (acquire;
-// bounded, and suspended in hardware rather than spinning on shared memory) and ORs the four
-// votes into *any. A vote slot of phase e is rewritten only in phase e + 2, after every warp has
-// passed e + 1.
-__device__ __forceinline__ int group_arrive(const Ctx& ctx, int g, int wq, int& epoch, bool vote) {
-    const int e = epoch++;
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) {
-        ctx.sm->gvote[g][e & 1][wq] = vote ? 1 : 0;
-        mbar_arrive(smem_u32(&ctx.sm->gbar[g]));
-    }
-    return e;
+// Hardware barrier of one softmax warpgroup (named barrier 1 + g, its 128 threads), optionally
+// OR-reducing a predicate over them. Every warp of the group runs every tile (a failed wait
+// skips work, never the loop), so each barrier is always reached by all four warps.
+__device__ __forceinline__ bool group_vote(int g, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pv, pr;\n\t"
+        "setp.ne.u32 pv, %1, 0;\n\t"
+        "bar.red.or.pred pr, %2, 128, pv;\n\t"
+        "selp.u32 %0, 1, 0, pr;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u), "r"(1 + g)
+        : "memory");
+    return r != 0;
 }
-__device__ __forceinline__ bool group_wait(const Ctx& ctx, int g, int e, bool* any) {
-    const bool ok = ctx.wait_warp(&ctx.sm->gbar[g], e & 1);
-    if (any) {
-        const volatile int* f = ctx.sm->gvote[g][e & 1];
-        *any = ok && (f[0] | f[1] | f[2] | f[3]) != 0;
-    }
-    return ok;
-}
-__device__ __forceinline__ bool group_sync(const Ctx& ctx, int g, int wq, int& epoch, bool vote,
-                                           bool* any) {
-    return group_wait(ctx, g, group_arrive(ctx, g, wq, epoch, vote), any);
+__device__ __forceinline__ void group_bar(int g) {
+    asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory");
 }
 
 // (pool row, clamped?) of key j0 of sequence b from the block table, for splits longer than the
@@ -436,7 +428,6 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         mbar_init(smem_u32(&sm.vtail), 1);
         mbar_init(smem_u32(&sm.odone), 1);
         mbar_init(smem_u32(&sm.qready), C::kSoftWarps);
-        for (int i = 0; i < C::kGroups; ++i) mbar_init(smem_u32(&sm.gbar[i]), 4);
         sm.abort = 0;
         fence_mbar_init();
     }
@@ -799,7 +790,6 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sm.qready));
         }
-        int epoch = 0;
         bool alive = ctx.wait_warp(&sm.qready, 0);
         // Per-row score scale and s minus the reference max live in shared memory (read as pairs
         // of 64-bit words, identical for every thread of the group). Scores, exponents, row sums
@@ -822,13 +812,10 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         const uint64_t k16th = pk2(0.0625f, 0.0625f), k256th = pk2(0.00390625f, 0.00390625f);
         const uint64_t k16 = pk2(16.f, 16.f);
         constexpr uint64_t kTrunc4 = 0xFFF00000FFF00000ull;  // sign, exponent, 3 mantissa bits
-        for (int t = 0; alive && t < ntiles; ++t) {
+        for (int t = 0; t < ntiles; ++t) {
             const int tile0 = start + t * kTile;
             const int j = tile0 + st;
-            if (!ctx.wait_lane0(&sm.sfull, t & 1)) {
-                alive = false;
-                break;
-            }
+            if (alive && !ctx.wait_lane0(&sm.sfull, t & 1)) alive = false;
             tc_fence_after();
             // y = (S0 + S1/16 + S2/256) * c0: the score in log2 units
             uint64_t y[kGroupRows / 2];
@@ -849,7 +836,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sm.sempty));  // S free for QK(t+1)
+            if (lane == 0 && alive) mbar_arrive(smem_u32(&sm.sempty));  // S free for QK(t+1)
             uint32_t validm = rowmask;  // bit i: key j visible to row row0 + i
             if (!((tile0 + kTile <= end) && (tile0 + kTile - 1 <= qoff))) {
                 // row r of the slot (query token r / G) sees key j iff r / G >= j - qoff, that is
@@ -922,11 +909,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             };
             // tile 0 always sets the reference max; later tiles vote on whether to move it
             bool need_any = true;
-            if (t > 0 &&
-                !group_sync(ctx, g, wq, epoch, __any_sync(0xffffffffu, need), &need_any)) {
-                alive = false;
-                break;
-            }
+            if (t > 0) need_any = group_vote(g, need);
             bool ok = true;
             if (need_any) {
                 // exact tile maximum per row -> new reference max; rescale row sums and O. The
@@ -954,10 +937,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                     v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
                     if ((lane & 1) == 0) sm.rmax[g][wq][lane >> 1] = v[0];
                 }
-                if (!group_sync(ctx, g, wq, epoch, false, nullptr)) {
-                    alive = false;
-                    break;
-                }
+                group_bar(g);
                 const int ri = (lane >> 1) & (kGroupRows - 1);
                 const float mo = kPShift - sm.nmcur[g][wq][ri];
                 const float tm = fmaxf(fmaxf(sm.rmax[g][0][ri], sm.rmax[g][1][ri]),
@@ -982,7 +962,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                     // the last V stage of tile t-1 done means all of it), then scale this
                     // group's row columns of all three terms in both head-dim halves
                     const int ul = (kTile / kVKeys) * t - 1;
-                    ok = ctx.wait_warp(&sm.vfree[ul % kVStages], (ul / kVStages) & 1);
+                    ok = alive && ctx.wait_warp(&sm.vfree[ul % kVStages], (ul / kVStages) & 1);
                     if (ok) {
                         tc_fence_after();
 #pragma unroll 1
@@ -1010,14 +990,12 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
             for (int q = 0; q < kGroupRows / 2; ++q) lsum[q] = add2(lsum[q], pv[q]);
             // this warp's keys of P are free once the V stage that consumed them in tile t-1
             // is done
-            if (ok && t > 0) {
+            if (alive && ok && t > 0) {
                 const int u = (kTile / kVKeys) * (t - 1);
                 ok = ctx.wait_warp(&sm.vfree[u % kVStages], (u / kVStages) & 1);
             }
-            if (!ok) {
-                alive = false;
-                break;
-            }
+            if (!ok) alive = false;
+            if (!alive) continue;  // every warp still runs the remaining tiles' barriers
             uint8_t* pbuf = smem + C::kOffP;
 #pragma unroll
             for (int term = 0; term < kTerms; ++term)
@@ -1059,7 +1037,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                 }
             }
         }
-        if (alive) alive = group_sync(ctx, g, wq, epoch, false, nullptr);
+        group_bar(g);
         const int64_t unit = slot;  // this split's workspace slot
         // lane i of the group's first warp writes row i (a compact block: this code runs once per
         // CTA, from a cold instruction cache)
