@@ -190,20 +190,13 @@ struct Ctx {
         atomicOr(status, DFLASH_FLAG_KERNEL_TIMEOUT);
         return false;
     }
-    // The same for code run by a whole warp: every lane waits, and the warp agrees on the result,
-    // so that no later warp-synchronous instruction runs with part of the warp gone. For waits
-    // after which the lanes read data the async proxy wrote (TMA copies).
+    // The same for code run by a whole warp: every lane waits (the hardware suspends and wakes
+    // the warp as one; a wait by lane 0 with the others held at a shuffle measured slower), and
+    // the warp agrees on the result, so that no later warp-synchronous instruction runs with part
+    // of the warp gone.
     __device__ bool wait_warp(uint64_t* bar, uint32_t parity) const {
         const bool ok = wait(bar, parity);
         return __all_sync(0xffffffffu, ok);
-    }
-    // A whole warp's wait carried out by lane 0 alone, the result broadcast to the warp. For waits
-    // that order a buffer's reuse or precede tensor-memory loads (tcgen05.fence::after_thread_sync
-    // follows).
-    __device__ bool wait_lane0(uint64_t* bar, uint32_t parity) const {
-        bool ok = true;
-        if ((threadIdx.x & 31) == 0) ok = wait(bar, parity);
-        return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     }
     __device__ bool aborted() const { return *reinterpret_cast<volatile int*>(&sm->abort) != 0; }
 };
@@ -815,7 +808,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         for (int t = 0; t < ntiles; ++t) {
             const int tile0 = start + t * kTile;
             const int j = tile0 + st;
-            if (alive && !ctx.wait_lane0(&sm.sfull, t & 1)) alive = false;
+            if (alive && !ctx.wait_warp(&sm.sfull, t & 1)) alive = false;
             tc_fence_after();
             // y = (S0 + S1/16 + S2/256) * c0: the score in log2 units
             uint64_t y[kGroupRows / 2];
