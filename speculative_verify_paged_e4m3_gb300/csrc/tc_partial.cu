@@ -840,17 +840,16 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                 else if (first > 0)
                     validm &= first >= kGroupRows ? 0u : (0xFFFFFFFFu << first);
             }
-            // e = y + (s - m): the exponent of the shifted probability; would any visible one
-            // exceed 2^8?
+            // e = y c0 + (s - m): the exponent of the shifted probability, one fused multiply-add
+            // (the scaled score y c0 itself is formed only on the reference-max path); would any
+            // visible one exceed 2^8?
             uint64_t e[kGroupRows / 2];
             bool need = false;
 #pragma unroll
             for (int i4 = 0; i4 < kGroupRows / 4; ++i4) {
                 const ulonglong2 c = c0v[i4];
-                y[2 * i4] = mul2(y[2 * i4], c.x);
-                y[2 * i4 + 1] = mul2(y[2 * i4 + 1], c.y);
-                e[2 * i4] = add2(y[2 * i4], nm[2 * i4]);
-                e[2 * i4 + 1] = add2(y[2 * i4 + 1], nm[2 * i4 + 1]);
+                e[2 * i4] = fma2(y[2 * i4], c.x, nm[2 * i4]);
+                e[2 * i4 + 1] = fma2(y[2 * i4 + 1], c.y, nm[2 * i4 + 1]);
             }
             // Every row of the group sees this key (all but the causal-window and ragged tiles):
             // the per-row visibility tests are skipped below.
@@ -910,6 +909,12 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                 // the group's through shared memory; lanes 2i and 2i + 1 then derive row i's new
                 // reference and weight, which the shuffles below hand to every lane (compact code:
                 // tile 0 runs it cold, later tiles rarely)
+#pragma unroll
+                for (int i4 = 0; i4 < kGroupRows / 4; ++i4) {  // the scaled scores
+                    const ulonglong2 c = c0v[i4];
+                    y[2 * i4] = mul2(y[2 * i4], c.x);
+                    y[2 * i4 + 1] = mul2(y[2 * i4 + 1], c.y);
+                }
                 {
                     float v[kGroupRows];
 #pragma unroll
