@@ -454,10 +454,14 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         // about 15 boxes a microsecond, an SM about 22, and a tile takes 32 (16-key chunks, two
         // 128-byte halves, K and V). Copier ci owns the K chunks c with c % 3 == ci and the V
         // chunks with c % 3 == (ci + 1) % 3, and arrives once per K tile and per V stage with the
-        // bytes of its own copies. Each copier polls both rings without blocking, K first (the
-        // scores come before the probabilities). A ragged last V stage is copied whole by copier
-        // 1, which zeroes its keys past the split's end once they have landed (P is zero there,
-        // but a stale NaN code times zero is NaN); the others only arrive on it.
+        // bytes of its own copies. The copiers take the stages in the order in which the MMAs
+        // release them: K tiles 0-2 and V stages 0-1 at once, then K tile t + 2 before V stage t
+        // (QK of tile t - 1 is issued, and so completes, before PV of tile t - 2). Each waits for
+        // its next stage with the hardware-suspended mbarrier wait instead of polling: the copier
+        // warps share their SM sub-partitions with softmax warps, whose issue slots polling
+        // takes, and a copy has more than a tile of slack. A ragged last V stage is copied whole
+        // by copier 1, which zeroes its keys past the split's end once they have landed (P is
+        // zero there, but a stale NaN code times zero is NaN); the others only arrive on it.
         const int ci = warp == 0 ? 0 : (warp == 2 ? 1 : 2);
         const uint64_t stream = l2_evict_first_policy();  // every page is read once
         constexpr int kChunks = kTile / kChunk;          // 8 per K tile and per V stage
@@ -486,20 +490,17 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
         }
         int tk = 0, tv = 0;
         bool tail_pending = false;  // the ragged stage's copies are issued but not awaited
-        uint64_t last = globaltimer_ns();
-        uint32_t idle = 0;
         while (tk < ntiles || tv < nvst) {
-            bool progressed = false;
-            bool kready = false, vready = false;
-            if (lane == 0) {
-                kready = tk < ntiles && mbar_test_wait(smem_u32(&sm.kempty[tk % kKStages]),
-                                                       ((tk / kKStages) & 1) ^ 1);
-                vready = tv < nvst && mbar_test_wait(smem_u32(&sm.vfree[tv % kVStages]),
-                                                     ((tv / kVStages) & 1) ^ 1);
+            // K tile tk next, or V stage tv (every lane waits for the stage's release, which
+            // also orders the tail's zeroing stores below after the MMAs that read the stage)
+            const bool k_next = tk < ntiles && (tv >= nvst || tk < kKStages ||
+                                                (tv >= kVStages && tk <= tv + 2));
+            if (k_next) {
+                if (!ctx.wait_warp(&sm.kempty[tk % kKStages], ((tk / kKStages) & 1) ^ 1)) break;
+            } else if (!ctx.wait_warp(&sm.vfree[tv % kVStages], ((tv / kVStages) & 1) ^ 1)) {
+                break;
             }
-            kready = __shfl_sync(0xffffffffu, kready, 0);
-            vready = __shfl_sync(0xffffffffu, vready, 0);
-            if (kready) {
+            if (k_next) {
                 if (lane == 0) {
                     if (!dep_done && start + (tk + 1) * kTile > drafted) {
                         griddep_wait();
@@ -521,9 +522,7 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                     if (tk + 1 < ntiles) own_rows(start + (tk + 1) * kTile, kfirst, krows);
                 }
                 ++tk;
-                progressed = true;
-            }
-            if (vready) {
+            } else {
                 const int vs = tv % kVStages;
                 const int h0 = start + tv * kVKeys;
                 const int nkeys = min(kVKeys, end - h0);
@@ -548,8 +547,6 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                         }
                     }
                 } else if (ci == 1) {
-                    // every lane acquires the stage's release before the zeroing stores below
-                    if (!ctx.wait_warp(&sm.vfree[vs], ((tv / kVStages) & 1) ^ 1)) break;
                     if (lane == 0) {
                         const int nval = (nkeys + kChunk - 1) / kChunk;  // chunks holding a key
                         const uint32_t bar = smem_u32(&sm.vtail);
@@ -582,20 +579,6 @@ __global__ void __launch_bounds__(Cfg<RP>::kThreads, 1)
                 }
                 if (lane == 0 && tv + 1 < nvst) own_rows(h0 + kVKeys, vfirst, vrows);
                 ++tv;
-                progressed = true;
-            }
-            if (progressed) {
-                idle = 0;
-                last = globaltimer_ns();
-            } else if ((++idle & 15) == 0) {
-                if (ctx.aborted()) break;
-                if (globaltimer_ns() - last > kWaitLimitNs) {
-                    if (lane == 0) {
-                        *reinterpret_cast<volatile int*>(&sm.abort) = 1;
-                        atomicOr(p.status, DFLASH_FLAG_KERNEL_TIMEOUT);
-                    }
-                    break;
-                }
             }
         }
         if (lane == 0) {
