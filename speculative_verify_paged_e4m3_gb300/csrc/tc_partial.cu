@@ -33,15 +33,17 @@
 //  * Warp roles: warps 0, 2 and 3 share the copies of K (TMA, 3 stages of 128 keys) and V (2
 //    stages), each a fixed third of every tile's 16-key page chunks; the last ragged V stage is
 //    copied whole by one of them, which zeroes its keys past the context (a zero probability must
-//    not meet a NaN code). Three K stages against two V stages: a K copy lands about 1.5 us after
-//    it is issued and tile t+3's copy waits for QK of tile t, while V of a tile is needed only
-//    after its softmax (with these rings the softmax warpgroups, not the copies, set the tile
-//    period at 48 rows). Warp 1 owns tensor memory and issues the MMAs from one thread that
-//    polls both streams (QK of the next tile, PV of the next V stage) without blocking on
-//    either; warps 4.. stage the Q terms (while the first copies are in flight), then run the
-//    softmax and write O out. The copies come from three warps: on this GPU the copy throughput
-//    of one SM grows with the number of warps issuing them (4.4, 6.2 and 6.6 TB/s over the
-//    whole GPU for one, two and three warps; two warps measured slower in this kernel too).
+//    not meet a NaN code). Three K stages against two V stages: a K copy lands about 2 us after
+//    it is issued under load and tile t+3's copy waits for QK of tile t, while V of a tile is
+//    needed only after its softmax (at 48 rows the softmax warpgroups and the V ring together
+//    set the tile period: V of tile t, copied once PV of tile t-2 is done, lands about as P of
+//    tile t is written; the other split, 2 K + 3 V, makes K late instead). Warp 1 owns tensor
+//    memory and issues the MMAs from one thread that polls both streams (QK of the next tile, PV
+//    of the next V stage) without blocking on either; warps 4.. stage the Q terms (while the
+//    first copies are in flight), then run the softmax and write O out. The copies come from
+//    three warps: on this GPU the copy throughput of one SM grows with the number of warps
+//    issuing them (4.4, 6.2 and 6.6 TB/s over the whole GPU for one, two and three warps; two
+//    warps measured slower in this kernel too).
 //  * One P buffer: the softmax warp of lane quadrant q writes keys [32q, 32q + 32) of every
 //    tile once the PV of the previous tile has read them; the PV of a tile waits for one
 //    barrier that every softmax warp arrives on (one test for the MMA thread to poll).
