@@ -63,6 +63,17 @@ def test_forced_split_counts(kernel, splits):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("tiles", range(1, 8))
+@pytest.mark.parametrize("delta", [-1, 0, 1])
+def test_single_split_tile_counts(kernel, tiles, delta):
+    # one split of 1..7 whole 128-key tiles, one key short of them, or one key over: the copies'
+    # start (three K tiles and two V stages at once), the order in which later stages are freed
+    # and refilled, and a ragged last V stage, at every tile count where those phases meet
+    n = max(8, 128 * tiles + delta)
+    check(small(f"tiles{tiles}_{delta}", [n], seed=400 + 3 * tiles + delta), kernel, num_splits=1)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("splits,n,P", [(1, 20000, 16), (2, 33000, 64), (3, 26000, 32)])
 def test_splits_longer_than_row_cache(kernel, splits, n, P):
     # more than 512 16-key chunks per split: chunks past the row cache come from the block table
